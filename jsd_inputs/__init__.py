@@ -1,0 +1,126 @@
+"""Seeded synthetic inputs for the fused-linear JSD loss.
+
+This module only draws random tensors of the right shapes, dtypes and
+structure; it holds none of the loss arithmetic. The same tensors are fed to
+the CUDA library and to the CPU oracle.
+
+Recipe (every workload): a torch generator seeded with the workload's seed
+draws, in this order, X_s [BT x H_s] ~ N(0, 1), W_s [V x H_s] ~ N(0, 1/H_s),
+X_t [BT x H_t] ~ N(0, 1) and W_t [V x H_t] ~ N(0, 1/H_t) in float32; each is
+then cast to the workload dtype. Labels come from a separate CPU generator with
+the same seed: uniform in [0, V), then the first floor(frac*BT) rows of a
+random permutation are set to ignore_index (-100).
+
+The hidden states and lm_head weights of a real model are not needed: the
+pages measure on synthetic shapes only (H=4096, V=128256, bf16).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+IGNORE_INDEX = -100
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    seed: int
+    bt: int
+    h_s: int
+    h_t: int
+    v: int
+    dtype: str  # "fp32" | "bf16"
+    beta: float = 0.5
+    temperature: float = 1.0
+    reduction: str = "batchmean"
+    ignore_frac: float = 0.0
+    tie: str = "none"  # "none" | "self" (X_t=X_s, W_t=W_s) | "padded"
+    pad_frac: float = 0.0  # fraction of trailing vocab rows zeroed in W_s and W_t
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "fp32" else torch.bfloat16
+
+    def flops(self) -> float:
+        """Dense FLOPs of one forward+backward: 2*BT*V*(3*H_s + H_t)."""
+        return 2.0 * self.bt * self.v * (3 * self.h_s + self.h_t)
+
+
+WORKLOADS = {
+    # tiny fp32 case the oracle finishes instantly
+    "tiny_fp32": Workload("tiny_fp32", 1, 64, 128, 128, 1000, "fp32"),
+    # self-distillation: every element ties
+    "ties_self": Workload("ties_self", 2, 1024, 4096, 4096, 32000, "bf16", tie="self"),
+    # independent teacher weights; the last 10% of vocab rows are zero in both
+    "ties_padded": Workload("ties_padded", 2, 1024, 4096, 4096, 32000, "bf16",
+                            tie="padded", pad_frac=0.1),
+    # multi-block vocabulary with a partial trailing block, 10% ignored rows
+    "multiblock": Workload("multiblock", 3, 2048, 2048, 2048, 40960, "bf16", ignore_frac=0.1),
+    # Llama-3-8B lm_head shape, 5% ignored rows
+    "llama3_lmhead": Workload("llama3_lmhead", 4, 4096, 4096, 4096, 128256, "bf16",
+                              ignore_frac=0.05),
+    # student H=4096, teacher H=8192
+    "large_teacher": Workload("large_teacher", 5, 8192, 4096, 8192, 128256, "bf16",
+                              beta=0.1, temperature=2.0, ignore_frac=0.05),
+    # the pages' benchmark shape: BT=8192, H=4096, V=128256, bf16
+    "headline": Workload("headline", 6, 8192, 4096, 4096, 128256, "bf16"),
+}
+
+
+def _randn(shape, std, gen, device):
+    t = torch.empty(shape, dtype=torch.float32, device=device)
+    t.normal_(0.0, std, generator=gen)
+    return t
+
+
+def make_labels(bt: int, v: int, ignore_frac: float, seed: int) -> torch.Tensor | None:
+    """int64 labels [BT]: uniform in [0, V); floor(frac*BT) rows set to -100."""
+    if ignore_frac <= 0.0:
+        return None
+    g = torch.Generator().manual_seed(seed)
+    labels = torch.randint(0, v, (bt,), generator=g, dtype=torch.int64)
+    n_ign = int(math.floor(ignore_frac * bt))
+    perm = torch.randperm(bt, generator=g)
+    labels[perm[:n_ign]] = IGNORE_INDEX
+    return labels
+
+
+def make_inputs(w: Workload, device: str = "cpu"):
+    """Draw (x_s, w_s, x_t, w_t, labels) for a workload on ``device``.
+
+    The float tensors are created on ``device`` (a CUDA generator is used for a
+    CUDA device, so the numbers differ from a CPU draw with the same seed, but
+    each draw is reproducible). Labels are always drawn on the CPU and moved.
+    """
+    gen = torch.Generator(device=device).manual_seed(w.seed)
+    x_s = _randn((w.bt, w.h_s), 1.0, gen, device)
+    w_s = _randn((w.v, w.h_s), 1.0 / math.sqrt(w.h_s), gen, device)
+    if w.tie == "self":
+        x_t, w_t = x_s, w_s
+    else:
+        x_t = x_s if w.tie == "padded" else _randn((w.bt, w.h_t), 1.0, gen, device)
+        w_t = _randn((w.v, w.h_t), 1.0 / math.sqrt(w.h_t), gen, device)
+    if w.pad_frac > 0.0:
+        first = w.v - int(round(w.pad_frac * w.v))
+        w_s[first:] = 0.0
+        w_t[first:] = 0.0
+    dt = w.torch_dtype
+    x_s, w_s = x_s.to(dt), w_s.to(dt)
+    if w.tie == "self":
+        x_t, w_t = x_s, w_s
+    else:
+        x_t = x_s if w.tie == "padded" else x_t.to(dt)
+        w_t = w_t.to(dt)
+    labels = make_labels(w.bt, w.v, w.ignore_frac, w.seed)
+    if labels is not None:
+        labels = labels.to(device)
+    return x_s, w_s, x_t, w_t, labels
+
+
+def custom(name: str, seed: int, bt: int, h_s: int, v: int, dtype: str = "bf16",
+           h_t: int | None = None, **kw) -> Workload:
+    """A workload of arbitrary shape with the same recipe (for small and odd shapes)."""
+    return Workload(name, seed, bt, h_s, h_s if h_t is None else h_t, v, dtype, **kw)

@@ -1,0 +1,282 @@
+"""Plain float64 CPU oracle for the fused-linear Jensen-Shannon distillation loss.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path may import this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use it. It shares no code with the CUDA library.
+
+What it computes, and the passages it follows (Liger-Kernel pull requests):
+
+* "[Perf] Fuse log-softmax into fused_linear_jsd kernel" (PR 1352), "Details":
+  the student and teacher logits are the two GEMMs X_s W_s^T and X_t W_t^T; both
+  log-softmaxes are taken on the temperature-scaled logits; the per-row loss
+  is a sum over V (loss_1d has shape (BT,)); the gradient with respect to the
+  log-probabilities X (dX) is pushed through the log-softmax Jacobian with the
+  cross-column term dX_sum, and the result is the gradient of the student
+  logits.
+* Same page, "Testing Done": the beta branches -- 0.0 is forward KL, 0.1 and
+  0.5 are the generalized JSD, 1.0 is reverse KL.
+* Same page, "Open questions" 2: the temperature divides the logits once; no
+  T^2 factor anywhere.
+* "Fix TVD gradient at p == q" (PR 1374), "Summary": a distance whose
+  per-element derivative is zero at p == q must give an exactly zero
+  gradient there; transferred to the JSD as an exactly zero per-element
+  contribution where the student and teacher log-probabilities tie.
+* "perf(flce): write the weight-gradient product directly into grad_weight"
+  (PR 1429), "Summary": grad_weight is the sum over row chunks of
+  dlogits^T . X_s.
+
+Readings where the pages are silent (each is listed with its reason in the
+design notes of the repository):
+
+* P is the teacher distribution, Q the student one. X = log Q, Y = log P.
+  beta = 0 gives KL(P||Q), beta = 1 gives KL(Q||P), and 0 < beta < 1 gives
+  beta*KL(P||M) + (1-beta)*KL(Q||M) with M = beta*P + (1-beta)*Q.
+* The endpoints are exact compares (beta == 0.0, beta == 1.0).
+* Reductions: sum (w = 1), batchmean (w = 1/n, n = rows whose label is not
+  ignore_index), mean (w = 1/(n*V)), none (per-row vector, the gradient is
+  that of sum_r row_grad[r]*L_r). With n == 0 the loss and every gradient are 0.
+* Rows whose label equals ignore_index contribute 0 to the loss and have a
+  zero gradient.
+* The tie rule sets the per-element loss to 0 in every branch where X_j == Y_j
+  exactly, and also the per-element log-probability gradient of the
+  generalized branch (whose exact value is 0 there). The endpoint branches
+  use closed-form logit gradients (Q - P at beta = 0, Q*(X - Y - L) at
+  beta = 1), which are exactly what the calculus gives at a tie.
+
+Every array is float64. Inputs are the exact values of the bf16/fp32 tensors,
+widened to float64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+REDUCTIONS = ("none", "sum", "mean", "batchmean")
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding (diagnostic only)
+# ---------------------------------------------------------------------------
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 value, ties to even, and widen to float64.
+
+    Used only by the ``emulate_rounding`` diagnostic: the fused kernel stores the
+    GEMM output in the input dtype ("Open questions" 1 of PR 1352) and writes
+    dlogits over the student logits buffer ("Details" of PR 1352), so with
+    bf16 inputs both round to bf16. The value is first rounded to float32
+    (nearest), then to bfloat16 (nearest, ties to even) by integer arithmetic
+    on the float32 bit pattern. NaN and infinity are not expected here.
+    """
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lower = u & np.uint64(0xFFFF)
+    upper = u >> np.uint64(16)
+    half = np.uint64(0x8000)
+    round_up = (lower > half) | ((lower == half) & ((upper & np.uint64(1)) == np.uint64(1)))
+    upper = upper + round_up.astype(np.uint64)
+    out = (upper << np.uint64(16)).astype(np.uint32).view(np.float32)
+    return out.astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# the two logits GEMMs
+# ---------------------------------------------------------------------------
+def logits(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """z = x . w^T for x [rows x H] and the lm_head weight w [V x H] (PR 1352,
+    "Summary": the logits are the product of hidden states and lm_head weight)."""
+    return np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+
+
+def log_softmax_rows(a: np.ndarray) -> np.ndarray:
+    """Row-wise log-softmax a - logsumexp(a), with the max subtracted first."""
+    m = np.max(a, axis=1, keepdims=True)
+    lse = m + np.log(np.sum(np.exp(a - m), axis=1, keepdims=True))
+    return a - lse
+
+
+# ---------------------------------------------------------------------------
+# per-row JSD and its gradient with respect to the scaled student logits
+# ---------------------------------------------------------------------------
+def jsd_rows(z_s: np.ndarray, z_t: np.ndarray, beta: float, temperature: float):
+    """Per-row loss L_r (shape [rows]) and dA = dL_r/da (shape [rows x V]).
+
+    a = z_s / T and b = z_t / T are the scaled logits (PR 1352, "Open
+    questions" 2: divide once). X = log_softmax(a) is the student log-prob
+    (log Q), Y = log_softmax(b) the teacher log-prob (log P). The branches
+    follow PR 1352 "Testing Done" (0.0 forward KL, 1.0 reverse KL, otherwise
+    generalized). For the generalized branch, dX_j = (1-beta) Q_j (X_j - log M_j)
+    is the gradient with respect to the log-prob and the logit gradient is
+    dX_j - Q_j * dX_sum (PR 1352, "Details": dX_sum is a cross-column term).
+    The tie rule of PR 1374 "Summary" zeroes the per-element contribution
+    where X_j == Y_j.
+    """
+    if temperature <= 0:
+        raise ValueError("temperature must be > 0")
+    if not (0.0 <= beta <= 1.0):
+        raise ValueError("beta must be in [0, 1]")
+    a = np.asarray(z_s, dtype=np.float64) / temperature
+    b = np.asarray(z_t, dtype=np.float64) / temperature
+    X = log_softmax_rows(a)
+    Y = log_softmax_rows(b)
+    Q = np.exp(X)
+    P = np.exp(Y)
+    tie = X == Y
+    if beta == 0.0:
+        # forward KL(P || Q)
+        ell = np.where(tie, 0.0, P * (Y - X))
+        L = ell.sum(axis=1)
+        dA = Q - P
+    elif beta == 1.0:
+        # reverse KL(Q || P)
+        ell = np.where(tie, 0.0, Q * (X - Y))
+        L = ell.sum(axis=1)
+        dA = Q * (X - Y - L[:, None])
+    else:
+        M = beta * P + (1.0 - beta) * Q
+        # where P and Q both underflow to 0 the terms are 0 * log 0 = 0
+        zero = tie | (M == 0.0)
+        logM = np.log(np.where(M == 0.0, 1.0, M))
+        ell = beta * P * (Y - logM) + (1.0 - beta) * Q * (X - logM)
+        ell = np.where(zero, 0.0, ell)
+        dX = np.where(zero, 0.0, (1.0 - beta) * Q * (X - logM))
+        L = ell.sum(axis=1)
+        dX_sum = dX.sum(axis=1)
+        dA = dX - Q * dX_sum[:, None]
+    return L, dA
+
+
+# ---------------------------------------------------------------------------
+# the whole fused-linear JSD forward + backward
+# ---------------------------------------------------------------------------
+def row_weights(labels, bt: int, v: int, reduction: str, ignore_index: int = -100,
+                row_grad=None):
+    """Per-row loss weights w_r and the valid-row count n.
+
+    Reading of the reductions (the pages name four reductions in PR 1374
+    "Details" and pin "batchmean" as division by the row count in the tie
+    table of PR 1374): sum -> 1, batchmean -> 1/n, mean -> 1/(n*V),
+    none -> row_grad[r] (1 when absent). Ignored rows get weight 0.
+    """
+    if reduction not in REDUCTIONS:
+        raise ValueError(f"unknown reduction {reduction!r}")
+    if labels is None:
+        valid = np.ones(bt, dtype=bool)
+    else:
+        valid = np.asarray(labels).reshape(-1) != ignore_index
+    n = int(valid.sum())
+    if reduction == "none":
+        rg = np.ones(bt) if row_grad is None else np.asarray(row_grad, dtype=np.float64)
+        w = np.where(valid, rg, 0.0)
+    elif n == 0:
+        w = np.zeros(bt)
+    elif reduction == "sum":
+        w = valid.astype(np.float64)
+    elif reduction == "batchmean":
+        w = valid / float(n)
+    else:  # mean
+        w = valid / (float(n) * float(v))
+    return w, valid, n
+
+
+def fljsd_ref(x_s, w_s, x_t, w_t, labels=None, *, beta: float = 0.5,
+              temperature: float = 1.0, reduction: str = "batchmean",
+              ignore_index: int = -100, row_grad=None, emulate_rounding: bool = False,
+              block_rows: int = 256):
+    """Loss, grad_input (d/dX_s) and grad_weight (d/dW_s) of the fused-linear JSD.
+
+    Rows are processed in blocks of ``block_rows`` only to bound memory; each row
+    is independent of the others except through the valid-row count n.
+    grad_weight is the sum over blocks of dz^T . X_s (PR 1429, "Summary").
+
+    With ``emulate_rounding`` the logits and dlogits are rounded to bf16 as the
+    bf16 kernels store them (PR 1352, "Open questions" 1 and "Details"); it is
+    a diagnostic, not the definition.
+
+    Returns (loss, grad_input, grad_weight): loss is a float for sum, mean and
+    batchmean, and a [BT] array for none.
+    """
+    x_s = np.asarray(x_s, dtype=np.float64)
+    w_s = np.asarray(w_s, dtype=np.float64)
+    x_t = np.asarray(x_t, dtype=np.float64)
+    w_t = np.asarray(w_t, dtype=np.float64)
+    bt, h_s = x_s.shape
+    v = w_s.shape[0]
+    assert w_s.shape == (v, h_s) and x_t.shape[0] == bt and w_t.shape == (v, x_t.shape[1])
+    w, valid, n = row_weights(labels, bt, v, reduction, ignore_index, row_grad)
+    loss_rows = np.zeros(bt)
+    grad_input = np.zeros((bt, h_s))
+    grad_weight = np.zeros((v, h_s))
+    for r0 in range(0, bt, block_rows):
+        r1 = min(bt, r0 + block_rows)
+        zs = logits(x_s[r0:r1], w_s)
+        zt = logits(x_t[r0:r1], w_t)
+        if emulate_rounding:
+            zs = bf16_round(zs)
+            zt = bf16_round(zt)
+        L, dA = jsd_rows(zs, zt, beta, temperature)
+        vb = valid[r0:r1]
+        L = np.where(vb, L, 0.0)
+        loss_rows[r0:r1] = L
+        dz = dA * (w[r0:r1] / temperature)[:, None]
+        dz[~vb] = 0.0
+        if emulate_rounding:
+            dz = bf16_round(dz)
+        grad_input[r0:r1] = dz @ w_s
+        grad_weight += dz.T @ x_s[r0:r1]
+    if reduction == "none":
+        loss = loss_rows
+    elif n == 0:
+        loss = 0.0
+    elif reduction == "sum":
+        loss = float(loss_rows.sum())
+    elif reduction == "batchmean":
+        loss = float(loss_rows.sum() / n)
+    else:
+        loss = float(loss_rows.sum() / (n * v))
+    return loss, grad_input, grad_weight
+
+
+def fljsd_rows_ref(x_s_rows, w_s, x_t_rows, w_t, *, beta: float, temperature: float,
+                   row_scale):
+    """Per-row loss L_r and grad_input rows for a sample of rows.
+
+    Each row of the method is independent once its weight w_r is known
+    (PR 1352, "Details": the kernel works row by row over V), so a sample of
+    rows can be checked at any problem size. ``row_scale`` is w_r for each
+    sampled row (for batchmean 1/n of the whole problem). Returns (L, dz,
+    grad_input_rows).
+    """
+    zs = logits(x_s_rows, w_s)
+    zt = logits(x_t_rows, w_t)
+    L, dA = jsd_rows(zs, zt, beta, temperature)
+    dz = dA * (np.asarray(row_scale, dtype=np.float64) / temperature)[:, None]
+    return L, dz, dz @ np.asarray(w_s, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# total variation distance (adjacent path; pins the batchmean reading)
+# ---------------------------------------------------------------------------
+def tvd_ref(p: np.ndarray, q: np.ndarray, reduction: str = "batchmean"):
+    """TVD loss 0.5*|p - q| summed over the vocabulary and its gradient in p.
+
+    "Fix TVD gradient at p == q" (PR 1374), "Summary": the derivative of
+    0.5*|p - q| is +0.5 where p > q, -0.5 where p < q, and exactly 0 at p == q
+    (the three-way sign). Reductions follow the same readings as the JSD; the
+    tie table of that page fixes batchmean as division by the number of rows.
+    Returns (loss, grad_p).
+    """
+    p = np.asarray(p, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    rows, v = p.shape
+    per_elem = 0.5 * np.abs(p - q)
+    sign = np.where(p > q, 1.0, np.where(p < q, -1.0, 0.0))
+    if reduction == "none":
+        return per_elem, 0.5 * sign
+    if reduction == "sum":
+        scale = 1.0
+    elif reduction == "batchmean":
+        scale = 1.0 / rows
+    elif reduction == "mean":
+        scale = 1.0 / (rows * v)
+    else:
+        raise ValueError(reduction)
+    return float(per_elem.sum() * scale), 0.5 * sign * scale

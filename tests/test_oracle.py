@@ -1,0 +1,334 @@
+"""Pins for the float64 CPU oracle: each test checks it against something other
+than its own formulas -- library routines, textbook closed forms, brute force in
+pure Python, finite differences, invariants of the mathematics, and the one
+value the pages print (the TVD tie table)."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import bf16_round, fljsd_ref, jsd_rows, row_weights, tvd_ref
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+BETAS = (0.0, 0.1, 0.5, 1.0)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _problem(seed, bt=4, h=8, v=16, h_t=None, scale=1.0):
+    r = _rng(seed)
+    h_t = h if h_t is None else h_t
+    x_s = r.standard_normal((bt, h)) * scale
+    w_s = r.standard_normal((v, h)) / math.sqrt(h)
+    x_t = r.standard_normal((bt, h_t)) * scale
+    w_t = r.standard_normal((v, h_t)) / math.sqrt(h_t)
+    return x_s, w_s, x_t, w_t
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding helper
+# ---------------------------------------------------------------------------
+def test_bf16_round_known_values():
+    # ulp(1) in bf16 is 2^-7; halfway cases round to the even neighbour.
+    x = np.array([1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -8 + 2 ** -20, -2.5, 0.0,
+                  3.0e38, 1e-40])
+    got = bf16_round(x)
+    assert got[0] == 1.0
+    assert got[1] == 1.0                      # tie -> even (mantissa 0)
+    assert got[2] == 1 + 2 ** -6              # tie -> even (mantissa 2)
+    assert got[3] == 1 + 2 ** -7              # above half -> up
+    assert got[4] == -2.5 and got[5] == 0.0
+
+
+def test_bf16_round_matches_torch_conversion():
+    x = _rng(0).standard_normal(100000) * np.exp(_rng(1).uniform(-20, 20, 100000))
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(bf16_round(x), ref)
+
+
+# ---------------------------------------------------------------------------
+# library routines and textbook forms at the endpoints
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T", [1.0, 2.0])
+def test_beta0_is_forward_kl_of_library(T):
+    """beta=0 is KL(P||Q) with P the teacher: torch kl_div(input=log Q, target=log P)."""
+    x_s, _, x_t, _ = _problem(3, bt=6, h=11, v=11)
+    eye = np.eye(11)
+    loss, _, _ = fljsd_ref(x_s, eye, x_t, eye, beta=0.0, temperature=T, reduction="batchmean")
+    logq = torch.log_softmax(torch.from_numpy(x_s / T), dim=-1)
+    logp = torch.log_softmax(torch.from_numpy(x_t / T), dim=-1)
+    ref = torch.nn.functional.kl_div(logq, logp, log_target=True, reduction="batchmean").item()
+    assert loss == pytest.approx(ref, rel=1e-12, abs=1e-15)
+
+
+@pytest.mark.parametrize("T", [1.0, 3.0])
+def test_beta1_is_reverse_kl_of_library(T):
+    """beta=1 is KL(Q||P): torch kl_div(input=log P, target=log Q)."""
+    x_s, _, x_t, _ = _problem(4, bt=5, h=9, v=9)
+    eye = np.eye(9)
+    loss, _, _ = fljsd_ref(x_s, eye, x_t, eye, beta=1.0, temperature=T, reduction="sum")
+    logq = torch.log_softmax(torch.from_numpy(x_s / T), dim=-1)
+    logp = torch.log_softmax(torch.from_numpy(x_t / T), dim=-1)
+    ref = torch.nn.functional.kl_div(logp, logq, log_target=True, reduction="sum").item()
+    assert loss == pytest.approx(ref, rel=1e-12)
+
+
+@pytest.mark.parametrize("T", [1.0, 2.0])
+def test_beta0_gradient_is_softmax_difference(T):
+    """Soft-target cross-entropy gradient: d/dz_s = (softmax(z_s/T) - softmax(z_t/T)) / T."""
+    from scipy.special import softmax
+
+    x_s, _, x_t, _ = _problem(5, bt=7, h=13, v=13)
+    eye = np.eye(13)  # logits == hidden states, so grad_input == dlogits
+    _, gi, _ = fljsd_ref(x_s, eye, x_t, eye, beta=0.0, temperature=T, reduction="sum")
+    ref = (softmax(x_s / T, axis=1) - softmax(x_t / T, axis=1)) / T
+    np.testing.assert_allclose(gi, ref, rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# brute force in pure Python: the entropy form of the generalized JSD
+# ---------------------------------------------------------------------------
+def _py_softmax(row):
+    m = max(row)
+    e = [math.exp(x - m) for x in row]
+    s = sum(e)
+    return [x / s for x in e]
+
+
+@pytest.mark.parametrize("beta", [0.1, 0.5, 0.9])
+def test_generalized_matches_entropy_form(beta):
+    """beta*KL(P||M) + (1-beta)*KL(Q||M) == H(M) - beta*H(P) - (1-beta)*H(Q),
+    evaluated with plain Python loops (no NumPy) on a tiny case."""
+    x_s, w_s, x_t, w_t = _problem(6, bt=3, h=5, v=7)
+    T = 1.5
+    loss_rows, _, _ = fljsd_ref(x_s, w_s, x_t, w_t, beta=beta, temperature=T, reduction="none")
+    for r in range(3):
+        zs = [sum(x_s[r][k] * w_s[j][k] for k in range(5)) / T for j in range(7)]
+        zt = [sum(x_t[r][k] * w_t[j][k] for k in range(5)) / T for j in range(7)]
+        q = _py_softmax(zs)
+        p = _py_softmax(zt)
+        m = [beta * pj + (1 - beta) * qj for pj, qj in zip(p, q)]
+
+        def ent(d):
+            return -sum(x * math.log(x) for x in d)
+
+        ref = ent(m) - beta * ent(p) - (1 - beta) * ent(q)
+        assert loss_rows[r] == pytest.approx(ref, rel=1e-10, abs=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# invariants
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("beta", BETAS)
+@pytest.mark.parametrize("T", [1.0, 2.0])
+@pytest.mark.parametrize("reduction", ["none", "sum", "mean", "batchmean"])
+def test_identical_student_teacher_gives_exact_zeros(beta, T, reduction):
+    x_s, w_s, _, _ = _problem(7, bt=6, h=12, v=40)
+    loss, gi, gw = fljsd_ref(x_s, w_s, x_s.copy(), w_s.copy(), beta=beta, temperature=T,
+                             reduction=reduction)
+    assert np.all(np.asarray(loss) == 0.0)
+    assert np.all(gi == 0.0) and np.all(gw == 0.0)
+
+
+@pytest.mark.parametrize("beta", [0.1, 0.3, 0.5])
+def test_beta_swap_symmetry(beta):
+    """JSD_beta(P, Q) == JSD_{1-beta}(Q, P); at beta=0.5 the loss is symmetric."""
+    r = _rng(8)
+    zs, zt = r.standard_normal((9, 50)) * 3, r.standard_normal((9, 50)) * 3
+    L1, _ = jsd_rows(zs, zt, beta, 1.0)
+    L2, _ = jsd_rows(zt, zs, 1.0 - beta, 1.0)
+    np.testing.assert_allclose(L1, L2, rtol=1e-12)
+
+
+@pytest.mark.parametrize("beta", [0.1, 0.5, 0.9])
+def test_bounds(beta):
+    """0 <= L_r <= h(beta) = -beta ln beta - (1-beta) ln(1-beta) (<= ln 2 at 0.5)."""
+    r = _rng(9)
+    zs, zt = r.standard_normal((64, 30)) * 20, r.standard_normal((64, 30)) * 20
+    L, _ = jsd_rows(zs, zt, beta, 1.0)
+    hb = -beta * math.log(beta) - (1 - beta) * math.log(1 - beta)
+    assert np.all(L >= 0.0) and np.all(L <= hb + 1e-12)
+    if beta == 0.5:
+        assert np.all(L <= math.log(2) + 1e-12)
+    # far-apart one-hot-like distributions approach the bound
+    zs1 = np.full((1, 4), -1e3); zs1[0, 0] = 0.0
+    zt1 = np.full((1, 4), -1e3); zt1[0, 1] = 0.0
+    L1, _ = jsd_rows(zs1, zt1, beta, 1.0)
+    assert L1[0] == pytest.approx(hb, rel=1e-9)
+
+
+def test_endpoint_limits():
+    """JSD_beta / beta -> KL(P||Q) as beta -> 0; JSD_beta / (1-beta) -> KL(Q||P) as beta -> 1."""
+    r = _rng(10)
+    zs, zt = r.standard_normal((5, 60)), r.standard_normal((5, 60))
+    eps = 1e-6
+    L_lo, _ = jsd_rows(zs, zt, eps, 1.0)
+    L_f, _ = jsd_rows(zs, zt, 0.0, 1.0)
+    L_hi, _ = jsd_rows(zs, zt, 1.0 - eps, 1.0)
+    L_r, _ = jsd_rows(zs, zt, 1.0, 1.0)
+    np.testing.assert_allclose(L_lo / eps, L_f, rtol=2e-5)
+    np.testing.assert_allclose(L_hi / eps, L_r, rtol=2e-5)
+    # and the endpoint losses are the textbook KLs, computed here with scipy
+    from scipy.special import rel_entr, softmax
+
+    q, p = softmax(zs, axis=1), softmax(zt, axis=1)
+    np.testing.assert_allclose(L_f, rel_entr(p, q).sum(axis=1), rtol=1e-11)
+    np.testing.assert_allclose(L_r, rel_entr(q, p).sum(axis=1), rtol=1e-11)
+
+
+@pytest.mark.parametrize("beta", BETAS)
+def test_shift_invariance_and_zero_row_sum(beta):
+    r = _rng(11)
+    zs, zt = r.standard_normal((6, 33)) * 2, r.standard_normal((6, 33)) * 2
+    L1, dA1 = jsd_rows(zs, zt, beta, 1.7)
+    L2, dA2 = jsd_rows(zs + 5.25, zt - 3.5, beta, 1.7)
+    np.testing.assert_allclose(L1, L2, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dA1, dA2, rtol=1e-8, atol=1e-13)
+    np.testing.assert_allclose(dA1.sum(axis=1), 0.0, atol=1e-14)
+
+
+@pytest.mark.parametrize("beta", BETAS)
+def test_temperature_rescaling(beta):
+    """L(x; T) == L(x/T; 1) and grad_input(T) == grad_input_at_1(x/T) / T."""
+    x_s, w_s, x_t, w_t = _problem(12, bt=5, h=6, v=20)
+    T = 2.5
+    l_t, gi_t, gw_t = fljsd_ref(x_s, w_s, x_t, w_t, beta=beta, temperature=T, reduction="sum")
+    l_1, gi_1, gw_1 = fljsd_ref(x_s / T, w_s, x_t / T, w_t, beta=beta, temperature=1.0,
+                                reduction="sum")
+    assert l_t == pytest.approx(l_1, rel=1e-12)
+    np.testing.assert_allclose(gi_t, gi_1 / T, rtol=1e-10, atol=1e-15)
+    np.testing.assert_allclose(gw_t, gw_1, rtol=1e-10, atol=1e-15)
+
+
+def test_ignored_rows_and_reductions():
+    x_s, w_s, x_t, w_t = _problem(13, bt=8, h=6, v=25)
+    labels = np.array([3, -100, 7, 0, -100, 24, 1, 2])
+    n = 6
+    out = {red: fljsd_ref(x_s, w_s, x_t, w_t, labels, beta=0.5, reduction=red)
+           for red in ("none", "sum", "mean", "batchmean")}
+    rows, gi_none, _ = out["none"]
+    assert rows[1] == 0.0 and rows[4] == 0.0
+    assert np.all(gi_none[1] == 0.0) and np.all(gi_none[4] == 0.0)
+    assert out["sum"][0] == pytest.approx(rows.sum(), rel=1e-13)
+    assert out["batchmean"][0] == pytest.approx(rows.sum() / n, rel=1e-13)
+    assert out["mean"][0] == pytest.approx(rows.sum() / (n * 25), rel=1e-13)
+    np.testing.assert_allclose(out["batchmean"][1] * n, out["sum"][1], rtol=1e-12)
+    # the content of ignored rows does not matter
+    x2 = x_s.copy(); x2[1] = 100.0
+    l2, gi2, gw2 = fljsd_ref(x2, w_s, x_t, w_t, labels, beta=0.5, reduction="batchmean")
+    assert l2 == out["batchmean"][0]
+    np.testing.assert_array_equal(gw2, out["batchmean"][2])
+    # every row ignored: zero loss and zero gradients, no NaN
+    lz, giz, gwz = fljsd_ref(x_s, w_s, x_t, w_t, np.full(8, -100), reduction="batchmean")
+    assert lz == 0.0 and np.all(giz == 0.0) and np.all(gwz == 0.0)
+
+
+def test_row_blocking_does_not_change_the_result():
+    x_s, w_s, x_t, w_t = _problem(14, bt=11, h=7, v=19)
+    a = fljsd_ref(x_s, w_s, x_t, w_t, beta=0.1, temperature=2.0, block_rows=256)
+    b = fljsd_ref(x_s, w_s, x_t, w_t, beta=0.1, temperature=2.0, block_rows=3)
+    assert a[0] == pytest.approx(b[0], rel=1e-13)
+    np.testing.assert_allclose(a[1], b[1], rtol=1e-12)
+    np.testing.assert_allclose(a[2], b[2], rtol=1e-11, atol=1e-16)
+
+
+# ---------------------------------------------------------------------------
+# central finite differences
+# ---------------------------------------------------------------------------
+def _scalar_loss(x_s, w_s, x_t, w_t, labels, beta, T, red, row_grad):
+    loss, _, _ = fljsd_ref(x_s, w_s, x_t, w_t, labels, beta=beta, temperature=T,
+                           reduction=red, row_grad=row_grad)
+    if red == "none":
+        return float(np.sum(np.asarray(row_grad) * loss))
+    return float(loss)
+
+
+@pytest.mark.parametrize("beta", [0.0, 0.1, 0.5, 1.0])
+@pytest.mark.parametrize("T", [1.0, 2.0])
+@pytest.mark.parametrize("red", ["none", "sum", "mean", "batchmean"])
+def test_finite_differences(beta, T, red):
+    x_s, w_s, x_t, w_t = _problem(100 + int(beta * 10) + int(T), bt=4, h=8, v=16)
+    labels = np.array([1, -100, 5, 2])
+    row_grad = np.array([0.7, 1.3, -0.4, 2.0]) if red == "none" else None
+    _, gi, gw = fljsd_ref(x_s, w_s, x_t, w_t, labels, beta=beta, temperature=T, reduction=red,
+                          row_grad=row_grad)
+    eps = 1e-6
+
+    def fd(arr, idx, which):
+        args = [x_s, w_s, x_t, w_t]
+        plus = [a.copy() for a in args]; minus = [a.copy() for a in args]
+        plus[which][idx] += eps; minus[which][idx] -= eps
+        return (_scalar_loss(*plus, labels, beta, T, red, row_grad)
+                - _scalar_loss(*minus, labels, beta, T, red, row_grad)) / (2 * eps)
+
+    num_gi = np.array([[fd(x_s, (i, j), 0) for j in range(8)] for i in range(4)])
+    num_gw = np.array([[fd(w_s, (i, j), 1) for j in range(8)] for i in range(16)])
+    for num, ana in ((num_gi, gi), (num_gw, gw)):
+        err = np.linalg.norm(num - ana) / max(np.linalg.norm(ana), 1e-30)
+        assert err <= 1e-6, err
+    assert np.all(gi[1] == 0.0)
+
+
+@pytest.mark.parametrize("beta", BETAS)
+def test_finite_differences_at_partial_ties(beta):
+    """Rows where most columns tie (the teacher is the student with two logits
+    swapped): the loss is smooth there, so finite differences give the true
+    gradient, which the tie rule must not disturb."""
+    r = _rng(15)
+    v = 12
+    x_s = r.standard_normal((3, v))
+    x_t = x_s.copy()
+    x_t[:, [2, 7]] = x_t[:, [7, 2]]
+    eye = np.eye(v)
+    _, gi, _ = fljsd_ref(x_s, eye, x_t, eye, beta=beta, temperature=1.0, reduction="sum")
+    eps = 1e-6
+    num = np.zeros_like(gi)
+    for i in range(3):
+        for j in range(v):
+            p, m = x_s.copy(), x_s.copy()
+            p[i, j] += eps; m[i, j] -= eps
+            lp, _, _ = fljsd_ref(p, eye, x_t, eye, beta=beta, reduction="sum")
+            lm, _, _ = fljsd_ref(m, eye, x_t, eye, beta=beta, reduction="sum")
+            num[i, j] = (lp - lm) / (2 * eps)
+    err = np.linalg.norm(num - gi) / np.linalg.norm(gi)
+    assert err <= 1e-6, err
+
+
+# ---------------------------------------------------------------------------
+# the printed value: the TVD tie table pins batchmean = divide by rows
+# ---------------------------------------------------------------------------
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = v
+    return vals
+
+
+def test_tvd_tie_table():
+    g = _golden("tvd_tie_batchmean.txt")
+    rows, vocab = int(g["rows"]), int(g["vocab"])
+    r = _rng(16)
+    p = r.dirichlet(np.ones(vocab), size=rows).astype(np.float32).astype(np.float64)
+    # p == q everywhere: every element is a tie and the gradient is exactly 0
+    _, grad = tvd_ref(p, p.copy(), reduction=g["reduction"])
+    assert np.all(grad == float(g["grad_at_tie_after_fix"]))
+    assert int(np.sum(grad != 0.0)) == int(g["wrong_elements_after"])
+    # the value a two-way split would have given at the tie (p < q branch)
+    # is the p < q gradient: -0.5 / rows
+    _, grad_lt = tvd_ref(p, p + 1e-3, reduction=g["reduction"])
+    assert np.all(grad_lt == float(g["grad_at_tie_before_fix"]))
+    assert int(np.sum(grad_lt != 0.0)) == int(g["wrong_elements_before"])
+
+
+def test_row_weights_reading():
+    w, valid, n = row_weights(np.array([1, -100, 2]), 3, 10, "mean")
+    assert n == 2 and list(valid) == [True, False, True]
+    np.testing.assert_allclose(w, [1 / 20, 0, 1 / 20])
