@@ -1,0 +1,192 @@
+/*
+ * fljsd.h -- C ABI of the GB300 (sm_103a) fused-linear Jensen-Shannon
+ * distillation loss.
+ *
+ * What the library computes (Liger-Kernel pull requests, cited by title):
+ *
+ *  - "[Perf] Fuse log-softmax into fused_linear_jsd kernel" (PR 1352),
+ *    "Summary" and "Details": for a chunk of C rows, the student logits
+ *    Z_s = X_s . W_s^T and the teacher logits Z_t = X_t . W_t^T are formed in
+ *    the input dtype; the temperature-scaled log-softmaxes of both come from a
+ *    three-pass online softmax over V (pass 1: running max m and denominator d
+ *    for student and teacher together; pass 2: per-row loss and the
+ *    cross-column term dX_sum; pass 3: the logit gradient dZ written in place
+ *    over the student logits buffer). All math after the GEMM is fp32.
+ *  - Same page, "Testing Done": beta == 0 is forward KL(P||Q), beta == 1 is
+ *    reverse KL(Q||P), anything between is the generalized JSD
+ *    beta*KL(P||M) + (1-beta)*KL(Q||M), M = beta*P + (1-beta)*Q, with P the
+ *    teacher and Q the student distribution.
+ *  - Same page, "Open questions" 2: the temperature divides the logits once.
+ *  - "Fix TVD gradient at p == q" (PR 1374), "Summary": an element where the
+ *    student and teacher log-probabilities tie contributes exactly zero.
+ *  - "perf(flce): write the weight-gradient product directly into
+ *    grad_weight" (PR 1429), "Summary" and "Changes": grad_input = dZ . W_s per
+ *    chunk and grad_weight = sum over chunks of dZ^T . X_s, written straight
+ *    into grad_weight; the first chunk overwrites (beta = 0), later chunks add
+ *    the fp32 product to the stored value and round once; the outputs may be
+ *    uninitialised (empty_like) because every element is written.
+ *
+ * Conventions for every entry point:
+ *  - Matrices are dense, row-major, contiguous. Element type is given by
+ *    fljsd_problem.dtype for X_s, W_s, X_t, W_t, grad_input and grad_weight.
+ *  - Device pointers are caller-owned; the library allocates and frees no
+ *    device memory. Every device pointer must be 16-byte aligned.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream). Argument checks are synchronous: on any error status
+ *    nothing has been launched, except FLJSD_ERR_CUDA, which reports a launch
+ *    failure after earlier launches of the same call may have been queued.
+ *  - Not re-entrant across threads for the same workspace; distinct
+ *    workspaces on distinct streams may run concurrently.
+ */
+#ifndef FLJSD_H
+#define FLJSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st* fljsd_stream_t;
+
+typedef enum {
+  FLJSD_OK = 0,
+  FLJSD_ERR_INVALID_ARG = 1, /* null pointer, bad size, beta or temperature, misalignment */
+  FLJSD_ERR_UNSUPPORTED = 2, /* valid but not handled, e.g. bf16 with H % 8 != 0 */
+  FLJSD_ERR_WORKSPACE = 3,   /* workspace smaller than the plan requires */
+  FLJSD_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  FLJSD_ERR_TIMEOUT = 5      /* a bounded device-side wait expired */
+} fljsd_status;
+
+typedef enum { FLJSD_F32 = 0, FLJSD_BF16 = 1 } fljsd_dtype;
+
+/* Reductions. The pages name four (PR 1374, "Details") and fix "batchmean"
+ * as division by the number of rows (PR 1374, tie table). n = number of rows
+ * whose label != ignore_index (BT when labels is NULL).
+ *   NONE:      loss[r] = L_r (0 for ignored rows); gradients are those of
+ *              sum_r row_grad[r] * L_r (row_grad NULL means all ones).
+ *   SUM:       loss = sum_r L_r.
+ *   MEAN:      loss = sum_r L_r / (n * V).
+ *   BATCHMEAN: loss = sum_r L_r / n.
+ * With n == 0 the loss and both gradients are 0. */
+typedef enum {
+  FLJSD_RED_NONE = 0,
+  FLJSD_RED_SUM = 1,
+  FLJSD_RED_MEAN = 2,
+  FLJSD_RED_BATCHMEAN = 3
+} fljsd_reduction;
+
+typedef struct {
+  int64_t bt;           /* rows (batch * sequence) */
+  int64_t h_s;          /* student hidden size */
+  int64_t h_t;          /* teacher hidden size */
+  int64_t v;            /* vocabulary size */
+  int32_t dtype;        /* fljsd_dtype of X_s, W_s, X_t, W_t and the gradients */
+  int32_t reduction;    /* fljsd_reduction */
+  float beta;           /* in [0, 1]; 0 and 1 select the KL endpoints exactly */
+  float temperature;    /* > 0 and finite; logits are divided by it once */
+  int64_t ignore_index; /* label value of rows that are skipped (Liger: -100) */
+  int64_t chunk_rows;   /* rows per chunk; 0 lets fljsd_plan choose */
+} fljsd_problem;
+
+typedef struct {
+  int64_t chunk_rows;     /* C: rows of one chunk */
+  int64_t num_chunks;     /* ceil(bt / C) */
+  int64_t ld;             /* row stride (elements) of the logits buffers, >= v */
+  size_t workspace_bytes; /* device bytes fljsd_forward needs */
+  size_t logits_bytes;    /* 2 * C * ld * sizeof(dtype): the two logits buffers */
+  size_t stats_bytes;     /* per-row and per-tile statistics */
+} fljsd_plan_t;
+
+/*
+ * fljsd_plan -- choose the chunk geometry and size the workspace.
+ *
+ * If problem->chunk_rows > 0 it is used (clamped to bt). Otherwise the largest
+ * chunk whose workspace fits in half of `free_hbm_bytes` is taken (a multiple
+ * of 128 rows unless it is all of bt); free_hbm_bytes == 0 means "no limit",
+ * i.e. one chunk. The pages found one chunk fastest and the fixed
+ * cdiv(V, H) heuristic mis-tuned for JSD (PR 1352, "Open questions" 4); live
+ * memory per chunk is the two logits tensors, 2 * C * V * s bytes (PR 1352,
+ * "Details", memory table), plus O(C) statistics and the (BT,) loss vector.
+ * Host only; launches nothing. Returns FLJSD_ERR_INVALID_ARG for a bad
+ * problem, FLJSD_ERR_UNSUPPORTED for shapes the kernels do not handle, and
+ * FLJSD_ERR_WORKSPACE if not even one row fits.
+ */
+fljsd_status fljsd_plan(const fljsd_problem* problem, size_t free_hbm_bytes,
+                        fljsd_plan_t* out);
+
+/*
+ * fljsd_forward -- loss and both gradients (upstream gradient 1).
+ *
+ *   x_s [bt x h_s], w_s [v x h_s], x_t [bt x h_t], w_t [v x h_t]: inputs
+ *       (device, dtype; never modified). The teacher is frozen: no teacher
+ *       gradient is produced.
+ *   labels [bt] int64 (device) or NULL: rows with label == ignore_index are
+ *       skipped.
+ *   row_grad [bt] fp32 (device) or NULL: upstream per-row gradient, used only
+ *       with FLJSD_RED_NONE (NULL = ones).
+ *   loss (device fp32): [1] for SUM, MEAN, BATCHMEAN; [bt] for NONE.
+ *   grad_input [bt x h_s] (device, dtype): d loss / d x_s.
+ *   grad_weight [v x h_s] (device, dtype): d loss / d w_s.
+ *   workspace (device), workspace_bytes >= plan->workspace_bytes.
+ *
+ * Every element of loss, grad_input and grad_weight is written. `plan` must
+ * come from fljsd_plan for the same problem.
+ */
+fljsd_status fljsd_forward(const fljsd_problem* problem, const fljsd_plan_t* plan,
+                           const void* x_s, const void* w_s, const void* x_t,
+                           const void* w_t, const int64_t* labels, const float* row_grad,
+                           float* loss, void* grad_input, void* grad_weight,
+                           void* workspace, size_t workspace_bytes, fljsd_stream_t stream);
+
+/*
+ * fljsd_backward -- scale the gradients computed by fljsd_forward by the
+ * upstream scalar gradient *grad_output (device fp32), in place, on `stream`.
+ * The forward already holds the gradients for an upstream gradient of 1
+ * (PR 1352, "Details": the gradient is written during the forward pass), so
+ * this is one elementwise pass over grad_input [bt x h_s] and grad_weight
+ * [v x h_s] that does nothing when *grad_output == 1.
+ */
+fljsd_status fljsd_backward(const fljsd_problem* problem, const float* grad_output,
+                            void* grad_input, void* grad_weight, fljsd_stream_t stream);
+
+/* Static, human-readable name of a status code. Never NULL. */
+const char* fljsd_status_string(fljsd_status status);
+
+/*
+ * Launch accounting and per-kernel timing (for benchmarks).
+ *
+ * fljsd_launch_count returns the number of kernels this library has launched
+ * in the process (all devices, all streams) since load or the last
+ * fljsd_launch_count_reset.
+ *
+ * fljsd_trace_enable(max_launches) turns on per-launch CUDA-event timing on
+ * the launching stream for up to max_launches launches (events are created on
+ * the current device); fljsd_trace_enable(0) turns it off and releases the
+ * events. fljsd_trace_read synchronises the recorded events and returns, for
+ * kernel class `kind` (FLJSD_KERNEL_*), the summed milliseconds and the number
+ * of recorded launches; fljsd_trace_reset forgets the recorded launches.
+ * These are process-global and not thread-safe.
+ */
+typedef enum {
+  FLJSD_KERNEL_GEMM_LOGITS = 0,      /* Z = X . W^T, student and teacher */
+  FLJSD_KERNEL_JSD_ROWS = 1,         /* the three passes over V */
+  FLJSD_KERNEL_GEMM_GRAD_INPUT = 2,  /* dZ . W_s */
+  FLJSD_KERNEL_GEMM_GRAD_WEIGHT = 3, /* dZ^T . X_s into grad_weight */
+  FLJSD_KERNEL_SMALL = 4,            /* row count, loss reduction, scaling */
+  FLJSD_KERNEL_NUM_KINDS = 5
+} fljsd_kernel_kind;
+
+int64_t fljsd_launch_count(void);
+void fljsd_launch_count_reset(void);
+fljsd_status fljsd_trace_enable(int32_t max_launches);
+fljsd_status fljsd_trace_reset(void);
+fljsd_status fljsd_trace_read(int32_t kind, double* total_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLJSD_H */

@@ -1,0 +1,22 @@
+"""GB300 (sm_103a) fused-linear Jensen-Shannon distillation loss.
+
+The compute path is libfljsd.so (CUDA kernels behind the C ABI declared in
+include/fljsd.h). This package is its binding: ``_lib`` mirrors the C entry
+points by name, ``api`` adds torch allocation and an autograd Function.
+"""
+from ._lib import (  # noqa: F401
+    FljsdError,
+    fljsd_backward,
+    fljsd_forward,
+    fljsd_launch_count,
+    fljsd_launch_count_reset,
+    fljsd_plan,
+    fljsd_status_string,
+    fljsd_trace_enable,
+    fljsd_trace_read,
+    fljsd_trace_reset,
+    make_problem,
+)
+from .api import FusedLinearJSD, fused_linear_jsd  # noqa: F401
+
+LIB_PATH = _lib.LIB_PATH

@@ -1,0 +1,126 @@
+"""Torch-facing wrapper of the C ABI: allocation of outputs and workspace, and an
+autograd Function. PyTorch supplies device memory and streams only; every step
+of the loss runs in libfljsd.so."""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import fljsd_backward, fljsd_forward, fljsd_plan, make_problem
+
+_DT = {torch.float32: "fp32", torch.bfloat16: "bf16"}
+
+
+def _check(name, t, dtype, device, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+class FusedLinearJSD:
+    """Plans one problem shape and keeps its workspace for repeated calls.
+
+    ``forward`` returns (loss, grad_input, grad_weight) for an upstream gradient
+    of 1; ``backward`` scales both gradients in place by a device scalar.
+    """
+
+    def __init__(self, bt, h_s, h_t, v, dtype=torch.bfloat16, *, beta=0.5, temperature=1.0,
+                 reduction="batchmean", ignore_index=-100, chunk_rows=0, device="cuda",
+                 free_hbm_bytes=None):
+        self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        self.dtype = dtype
+        self.reduction = reduction
+        self.problem = make_problem(bt, h_s, h_t, v, _DT[dtype], reduction, beta, temperature,
+                                    ignore_index, chunk_rows)
+        if free_hbm_bytes is None:
+            free_hbm_bytes = torch.cuda.mem_get_info(self.device)[0]
+        self.plan = fljsd_plan(self.problem, int(free_hbm_bytes))
+        self.workspace = torch.empty(self.plan.workspace_bytes, dtype=torch.uint8,
+                                     device=self.device)
+
+    @property
+    def shape(self):
+        p = self.problem
+        return p.bt, p.h_s, p.h_t, p.v
+
+    def alloc_outputs(self):
+        bt, h_s, _, v = self.shape
+        n_loss = bt if self.reduction == "none" else 1
+        loss = torch.empty(n_loss, dtype=torch.float32, device=self.device)
+        gi = torch.empty(bt, h_s, dtype=self.dtype, device=self.device)
+        gw = torch.empty(v, h_s, dtype=self.dtype, device=self.device)
+        return loss, gi, gw
+
+    def forward(self, x_s, w_s, x_t, w_t, labels=None, row_grad=None, out=None, stream=None):
+        bt, h_s, h_t, v = self.shape
+        dev = self.device
+        _check("x_s", x_s, self.dtype, dev, (bt, h_s))
+        _check("w_s", w_s, self.dtype, dev, (v, h_s))
+        _check("x_t", x_t, self.dtype, dev, (bt, h_t))
+        _check("w_t", w_t, self.dtype, dev, (v, h_t))
+        if labels is not None:
+            _check("labels", labels, torch.int64, dev, (bt,))
+        if row_grad is not None:
+            _check("row_grad", row_grad, torch.float32, dev, (bt,))
+        loss, gi, gw = self.alloc_outputs() if out is None else out
+        fljsd_forward(self.problem, self.plan, x_s, w_s, x_t, w_t, labels, row_grad, loss, gi,
+                      gw, self.workspace, stream=stream)
+        return loss, gi, gw
+
+    def backward(self, grad_output, grad_input, grad_weight, stream=None):
+        _check("grad_output", grad_output, torch.float32, self.device)
+        fljsd_backward(self.problem, grad_output, grad_input, grad_weight, stream=stream)
+        return grad_input, grad_weight
+
+
+class _FusedLinearJSDFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x_s, w_s, x_t, w_t, labels, beta, temperature, reduction, ignore_index,
+                chunk_rows):
+        bt, h_s = x_s.shape
+        runner = FusedLinearJSD(bt, h_s, x_t.shape[1], w_s.shape[0], x_s.dtype, beta=beta,
+                                temperature=temperature, reduction=reduction,
+                                ignore_index=ignore_index, chunk_rows=chunk_rows,
+                                device=x_s.device)
+        xs, ws, xt, wt = (t.detach().contiguous() for t in (x_s, w_s, x_t, w_t))
+        lab = None if labels is None else labels.contiguous()
+        loss, gi, gw = runner.forward(xs, ws, xt, wt, lab)
+        ctx.runner = runner
+        ctx.inputs = (xs, ws, xt, wt, lab)
+        ctx.save_for_backward(gi, gw)
+        return loss if reduction == "none" else loss.reshape(())
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        gi, gw = ctx.saved_tensors
+        runner = ctx.runner
+        if runner.reduction == "none":
+            # a per-row upstream gradient: run the forward again with it
+            rg = grad_out.detach().to(torch.float32).contiguous()
+            _, gi, gw = runner.forward(*ctx.inputs, row_grad=rg)
+        else:
+            g = grad_out.detach().to(torch.float32).reshape(1).contiguous()
+            runner.backward(g, gi, gw)
+        return gi, gw, None, None, None, None, None, None, None, None
+
+
+def fused_linear_jsd(x_s, w_s, x_t, w_t, labels=None, *, beta=0.5, temperature=1.0,
+                     reduction="batchmean", ignore_index=-100, chunk_rows=0):
+    """Generalized JSD distillation loss between student logits x_s.w_s^T and
+    teacher logits x_t.w_t^T, differentiable in x_s and w_s (the teacher is
+    frozen). Tensors are 2-D, contiguous, on one CUDA device, fp32 or bf16."""
+    return _FusedLinearJSDFunction.apply(x_s, w_s, x_t, w_t, labels, float(beta),
+                                         float(temperature), reduction, int(ignore_index),
+                                         int(chunk_rows))
+
+
+__all__ = ["FusedLinearJSD", "fused_linear_jsd", "_lib"]

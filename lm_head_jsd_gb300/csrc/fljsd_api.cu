@@ -1,0 +1,337 @@
+// C ABI of libfljsd.so: argument checks, the chunk planner, the chunk loop
+// of the forward pass, the backward scaling, status strings, launch
+// accounting and per-kernel event timing. Declarations and semantics are in
+// include/fljsd.h.
+#include "internal.cuh"
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+namespace fljsd {
+
+// ---------------------------------------------------------------------------
+// launch accounting and tracing
+// ---------------------------------------------------------------------------
+namespace {
+std::atomic<int64_t> g_launches{0};
+
+struct Trace {
+  std::mutex mu;
+  int max = 0;
+  int used = 0;
+  int open = -1;  // index of the launch whose start event was recorded
+  std::vector<cudaEvent_t> start, stop;
+  std::vector<int> kind;
+} g_trace;
+
+void trace_release() {
+  for (auto e : g_trace.start) cudaEventDestroy(e);
+  for (auto e : g_trace.stop) cudaEventDestroy(e);
+  g_trace.start.clear();
+  g_trace.stop.clear();
+  g_trace.kind.clear();
+  g_trace.max = g_trace.used = 0;
+  g_trace.open = -1;
+}
+}  // namespace
+
+void trace_begin(int kind, cudaStream_t st) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_trace.max == 0) return;
+  std::lock_guard<std::mutex> lk(g_trace.mu);
+  if (g_trace.used >= g_trace.max) return;
+  const int i = g_trace.used;
+  g_trace.kind[i] = kind;
+  cudaEventRecord(g_trace.start[i], st);
+  g_trace.open = i;
+}
+
+void trace_end(int kind, cudaStream_t st) {
+  if (g_trace.max == 0) return;
+  std::lock_guard<std::mutex> lk(g_trace.mu);
+  if (g_trace.open < 0 || g_trace.kind[g_trace.open] != kind) return;
+  cudaEventRecord(g_trace.stop[g_trace.open], st);
+  g_trace.used = g_trace.open + 1;
+  g_trace.open = -1;
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+inline size_t dtype_size(int dt) { return dt == FLJSD_BF16 ? 2 : 4; }
+
+struct Layout {
+  int64_t ld;
+  size_t zs, zt, loss_rows, misc, total, logits_bytes, stats_bytes;
+};
+
+Layout layout_for(const fljsd_problem& p, int64_t chunk_rows) {
+  Layout L{};
+  L.ld = (p.v + 7) / 8 * 8;
+  const size_t s = dtype_size(p.dtype);
+  const size_t zbytes = align_up((size_t)chunk_rows * (size_t)L.ld * s);
+  L.zs = 0;
+  L.zt = zbytes;
+  L.loss_rows = 2 * zbytes;
+  L.misc = L.loss_rows + align_up((size_t)p.bt * sizeof(float));
+  L.total = L.misc + kAlign;
+  L.logits_bytes = 2 * (size_t)chunk_rows * (size_t)L.ld * s;
+  L.stats_bytes = align_up((size_t)p.bt * sizeof(float)) + kAlign;
+  return L;
+}
+
+fljsd_status check_problem(const fljsd_problem* p) {
+  if (p == nullptr) return FLJSD_ERR_INVALID_ARG;
+  if (p->bt <= 0 || p->h_s <= 0 || p->h_t <= 0 || p->v <= 0) return FLJSD_ERR_INVALID_ARG;
+  if (p->dtype != FLJSD_F32 && p->dtype != FLJSD_BF16) return FLJSD_ERR_INVALID_ARG;
+  if (p->reduction < FLJSD_RED_NONE || p->reduction > FLJSD_RED_BATCHMEAN)
+    return FLJSD_ERR_INVALID_ARG;
+  if (!(p->beta >= 0.f && p->beta <= 1.f)) return FLJSD_ERR_INVALID_ARG;  // also rejects NaN
+  if (!(p->temperature > 0.f) || !std::isfinite(p->temperature)) return FLJSD_ERR_INVALID_ARG;
+  if (p->chunk_rows < 0) return FLJSD_ERR_INVALID_ARG;
+  // grid limits of the kernels (rows of a chunk and vocabulary tiles)
+  if (p->v > (int64_t)1 << 30 || p->bt > (int64_t)1 << 30) return FLJSD_ERR_UNSUPPORTED;
+  if (p->h_s > (int64_t)1 << 20 || p->h_t > (int64_t)1 << 20) return FLJSD_ERR_UNSUPPORTED;
+  return FLJSD_OK;
+}
+
+inline bool aligned16(const void* q) { return ((uintptr_t)q & 15u) == 0; }
+
+}  // namespace
+}  // namespace fljsd
+
+using namespace fljsd;
+
+extern "C" {
+
+const char* fljsd_status_string(fljsd_status s) {
+  switch (s) {
+    case FLJSD_OK: return "ok";
+    case FLJSD_ERR_INVALID_ARG: return "invalid argument";
+    case FLJSD_ERR_UNSUPPORTED: return "unsupported problem";
+    case FLJSD_ERR_WORKSPACE: return "workspace too small";
+    case FLJSD_ERR_CUDA: return "CUDA error";
+    case FLJSD_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+fljsd_status fljsd_plan(const fljsd_problem* p, size_t free_hbm_bytes, fljsd_plan_t* out) {
+  fljsd_status st = check_problem(p);
+  if (st != FLJSD_OK) return st;
+  if (out == nullptr) return FLJSD_ERR_INVALID_ARG;
+  int64_t c = 0;
+  if (p->chunk_rows > 0) {
+    c = p->chunk_rows < p->bt ? p->chunk_rows : p->bt;
+  } else if (free_hbm_bytes == 0) {
+    c = p->bt;
+  } else {
+    const size_t budget = free_hbm_bytes / 2;
+    const Layout one = layout_for(*p, 1);
+    const Layout zero = layout_for(*p, 0);
+    const size_t per_row = one.total - zero.total;  // upper bound per row (alignment included)
+    if (budget < one.total) return FLJSD_ERR_WORKSPACE;
+    int64_t fit = (int64_t)((budget - zero.total) / (per_row > 0 ? per_row : 1));
+    if (fit >= p->bt) {
+      c = p->bt;
+    } else {
+      c = fit / 128 * 128;
+      if (c == 0) c = fit;
+      while (c > 0 && layout_for(*p, c).total > budget) c -= (c > 128 ? 128 : 1);
+      if (c <= 0) return FLJSD_ERR_WORKSPACE;
+    }
+  }
+  const Layout L = layout_for(*p, c);
+  out->chunk_rows = c;
+  out->num_chunks = (p->bt + c - 1) / c;
+  out->ld = L.ld;
+  out->workspace_bytes = L.total;
+  out->logits_bytes = L.logits_bytes;
+  out->stats_bytes = L.stats_bytes;
+  return FLJSD_OK;
+}
+
+fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, const void* x_s,
+                           const void* w_s, const void* x_t, const void* w_t,
+                           const int64_t* labels, const float* row_grad, float* loss,
+                           void* grad_input, void* grad_weight, void* workspace,
+                           size_t workspace_bytes, fljsd_stream_t stream_) {
+  fljsd_status st = check_problem(p);
+  if (st != FLJSD_OK) return st;
+  if (plan == nullptr) return FLJSD_ERR_INVALID_ARG;
+  if (!x_s || !w_s || !x_t || !w_t || !loss || !grad_input || !grad_weight || !workspace)
+    return FLJSD_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_s, w_s, x_t, w_t, loss, grad_input, grad_weight, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return FLJSD_ERR_INVALID_ARG;
+  if ((labels && !aligned16(labels)) || (row_grad && !aligned16(row_grad)))
+    return FLJSD_ERR_INVALID_ARG;
+  const int64_t c = plan->chunk_rows;
+  if (c <= 0 || c > p->bt || (p->chunk_rows > 0 && c != (p->chunk_rows < p->bt ? p->chunk_rows : p->bt)))
+    return FLJSD_ERR_INVALID_ARG;
+  const Layout L = layout_for(*p, c);
+  if (plan->ld != L.ld || plan->workspace_bytes != L.total ||
+      plan->num_chunks != (p->bt + c - 1) / c)
+    return FLJSD_ERR_INVALID_ARG;
+  if (workspace_bytes < L.total) return FLJSD_ERR_WORKSPACE;
+
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* ws = static_cast<char*>(workspace);
+  void* zs = ws + L.zs;
+  void* zt = ws + L.zt;
+  float* loss_rows = p->reduction == FLJSD_RED_NONE ? loss : reinterpret_cast<float*>(ws + L.loss_rows);
+  int* n_valid = reinterpret_cast<int*>(ws + L.misc);
+  const size_t s = dtype_size(p->dtype);
+
+  cudaError_t e = launch_count_valid(labels, p->bt, p->ignore_index, n_valid, stream);
+  if (e != cudaSuccess) return FLJSD_ERR_CUDA;
+
+  for (int64_t chunk = 0; chunk * c < p->bt; ++chunk) {
+    const int64_t r0 = chunk * c;
+    const int64_t rows = (p->bt - r0) < c ? (p->bt - r0) : c;
+    const char* xs_c = static_cast<const char*>(x_s) + (size_t)r0 * p->h_s * s;
+    const char* xt_c = static_cast<const char*>(x_t) + (size_t)r0 * p->h_t * s;
+
+    // student and teacher logits, rounded to the input dtype
+    GemmArgs g{};
+    g.a = xs_c; g.sam = p->h_s; g.sak = 1;
+    g.b = w_s; g.sbn = p->h_s; g.sbk = 1;
+    g.c = zs; g.ldc = L.ld; g.m = rows; g.n = p->v; g.k = p->h_s; g.accumulate = 0;
+    trace_begin(FLJSD_KERNEL_GEMM_LOGITS, stream);
+    e = launch_gemm_simt(p->dtype, g, stream);
+    trace_end(FLJSD_KERNEL_GEMM_LOGITS, stream);
+    if (e != cudaSuccess) return FLJSD_ERR_CUDA;
+    g.a = xt_c; g.sam = p->h_t;
+    g.b = w_t; g.sbn = p->h_t;
+    g.c = zt; g.k = p->h_t;
+    trace_begin(FLJSD_KERNEL_GEMM_LOGITS, stream);
+    e = launch_gemm_simt(p->dtype, g, stream);
+    trace_end(FLJSD_KERNEL_GEMM_LOGITS, stream);
+    if (e != cudaSuccess) return FLJSD_ERR_CUDA;
+
+    // three passes over V; dlogits overwrite the student logits
+    JsdRowArgs ra{};
+    ra.zs = zs; ra.zt = zt; ra.ld = L.ld; ra.v = p->v; ra.rows = rows; ra.row0 = r0;
+    ra.labels = labels; ra.ignore_index = p->ignore_index;
+    ra.row_grad = p->reduction == FLJSD_RED_NONE ? row_grad : nullptr;
+    ra.n_valid = n_valid; ra.loss_rows = loss_rows; ra.reduction = p->reduction;
+    ra.beta = p->beta; ra.inv_temperature = 1.0f / p->temperature;
+    e = launch_jsd_rows(p->dtype, ra, stream);
+    if (e != cudaSuccess) return FLJSD_ERR_CUDA;
+
+    // grad_input rows of this chunk = dZ . W_s
+    GemmArgs gi{};
+    gi.a = zs; gi.sam = L.ld; gi.sak = 1;
+    gi.b = w_s; gi.sbn = 1; gi.sbk = p->h_s;
+    gi.c = static_cast<char*>(grad_input) + (size_t)r0 * p->h_s * s; gi.ldc = p->h_s;
+    gi.m = rows; gi.n = p->h_s; gi.k = p->v; gi.accumulate = 0;
+    trace_begin(FLJSD_KERNEL_GEMM_GRAD_INPUT, stream);
+    e = launch_gemm_simt(p->dtype, gi, stream);
+    trace_end(FLJSD_KERNEL_GEMM_GRAD_INPUT, stream);
+    if (e != cudaSuccess) return FLJSD_ERR_CUDA;
+
+    // grad_weight (+)= dZ^T . X_s; the first chunk overwrites
+    GemmArgs gw{};
+    gw.a = zs; gw.sam = 1; gw.sak = L.ld;
+    gw.b = xs_c; gw.sbn = 1; gw.sbk = p->h_s;
+    gw.c = grad_weight; gw.ldc = p->h_s;
+    gw.m = p->v; gw.n = p->h_s; gw.k = rows; gw.accumulate = chunk > 0 ? 1 : 0;
+    trace_begin(FLJSD_KERNEL_GEMM_GRAD_WEIGHT, stream);
+    e = launch_gemm_simt(p->dtype, gw, stream);
+    trace_end(FLJSD_KERNEL_GEMM_GRAD_WEIGHT, stream);
+    if (e != cudaSuccess) return FLJSD_ERR_CUDA;
+  }
+
+  if (p->reduction != FLJSD_RED_NONE) {
+    e = launch_reduce_loss(loss_rows, p->bt, p->v, p->reduction, n_valid, loss, stream);
+    if (e != cudaSuccess) return FLJSD_ERR_CUDA;
+  }
+  return FLJSD_OK;
+}
+
+fljsd_status fljsd_backward(const fljsd_problem* p, const float* grad_output, void* grad_input,
+                            void* grad_weight, fljsd_stream_t stream_) {
+  fljsd_status st = check_problem(p);
+  if (st != FLJSD_OK) return st;
+  if (!grad_output || !grad_input || !grad_weight) return FLJSD_ERR_INVALID_ARG;
+  if (!aligned16(grad_input) || !aligned16(grad_weight) || ((uintptr_t)grad_output & 3u))
+    return FLJSD_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (launch_scale(p->dtype, grad_input, p->bt * p->h_s, grad_output, stream) != cudaSuccess)
+    return FLJSD_ERR_CUDA;
+  if (launch_scale(p->dtype, grad_weight, p->v * p->h_s, grad_output, stream) != cudaSuccess)
+    return FLJSD_ERR_CUDA;
+  return FLJSD_OK;
+}
+
+int64_t fljsd_launch_count(void) { return g_launches.load(); }
+void fljsd_launch_count_reset(void) { g_launches.store(0); }
+
+fljsd_status fljsd_trace_enable(int32_t max_launches) {
+  std::lock_guard<std::mutex> lk(g_trace.mu);
+  trace_release();
+  if (max_launches < 0) return FLJSD_ERR_INVALID_ARG;
+  if (max_launches == 0) return FLJSD_OK;
+  g_trace.start.resize(max_launches);
+  g_trace.stop.resize(max_launches);
+  g_trace.kind.assign(max_launches, -1);
+  for (int i = 0; i < max_launches; ++i) {
+    if (cudaEventCreate(&g_trace.start[i]) != cudaSuccess ||
+        cudaEventCreate(&g_trace.stop[i]) != cudaSuccess) {
+      g_trace.start.resize(i);
+      g_trace.stop.resize(i);
+      trace_release();
+      return FLJSD_ERR_CUDA;
+    }
+  }
+  g_trace.max = max_launches;
+  return FLJSD_OK;
+}
+
+fljsd_status fljsd_trace_reset(void) {
+  std::lock_guard<std::mutex> lk(g_trace.mu);
+  g_trace.used = 0;
+  g_trace.open = -1;
+  return FLJSD_OK;
+}
+
+fljsd_status fljsd_trace_read(int32_t kind, double* total_ms, int64_t* launches) {
+  if (!total_ms || !launches || kind < 0 || kind >= FLJSD_KERNEL_NUM_KINDS)
+    return FLJSD_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_trace.mu);
+  double tot = 0.0;
+  int64_t n = 0;
+  for (int i = 0; i < g_trace.used; ++i) {
+    if (g_trace.kind[i] != kind) continue;
+    if (cudaEventSynchronize(g_trace.stop[i]) != cudaSuccess) return FLJSD_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_trace.start[i], g_trace.stop[i]) != cudaSuccess)
+      return FLJSD_ERR_CUDA;
+    tot += ms;
+    ++n;
+  }
+  *total_ms = tot;
+  *launches = n;
+  return FLJSD_OK;
+}
+
+}  // extern "C"

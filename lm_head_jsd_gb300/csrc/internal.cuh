@@ -1,0 +1,65 @@
+// Internal declarations shared by the translation units of libfljsd.so.
+// Nothing here is part of the C ABI (that is include/fljsd.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "fljsd.h"
+
+namespace fljsd {
+
+// ---------------------------------------------------------------------------
+// launch accounting / tracing (fljsd_api.cu)
+// ---------------------------------------------------------------------------
+void trace_begin(int kind, cudaStream_t st);
+void trace_end(int kind, cudaStream_t st);
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// ---------------------------------------------------------------------------
+// row kernels (rows.cu)
+// ---------------------------------------------------------------------------
+struct JsdRowArgs {
+  void* zs;              // [rows x ld] student logits in, dlogits out (dtype)
+  const void* zt;        // [rows x ld] teacher logits (dtype)
+  int64_t ld;            // row stride in elements (multiple of 8)
+  int64_t v;             // vocabulary size
+  int64_t rows;          // rows of this chunk
+  int64_t row0;          // global index of the first row of this chunk
+  const int64_t* labels; // [bt] or null
+  int64_t ignore_index;
+  const float* row_grad; // [bt] or null (reduction NONE only)
+  const int* n_valid;    // device scalar
+  float* loss_rows;      // [bt], indexed by global row
+  int reduction;
+  float beta;
+  float inv_temperature;
+};
+
+cudaError_t launch_count_valid(const int64_t* labels, int64_t bt, int64_t ignore_index,
+                               int* n_valid, cudaStream_t st);
+cudaError_t launch_jsd_rows(int dtype, const JsdRowArgs& a, cudaStream_t st);
+cudaError_t launch_reduce_loss(const float* loss_rows, int64_t bt, int64_t v, int reduction,
+                               const int* n_valid, float* loss, cudaStream_t st);
+cudaError_t launch_scale(int dtype, void* p, int64_t n, const float* g, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// GEMMs. C[m, n] (+)= sum_k A(m, k) * B(n, k), fp32 accumulation, one rounding
+// to the output dtype. A(m, k) = A[m * sam + k * sak], B(n, k) = B[n * sbn + k * sbk].
+// ---------------------------------------------------------------------------
+struct GemmArgs {
+  const void* a; int64_t sam, sak;
+  const void* b; int64_t sbn, sbk;
+  void* c; int64_t ldc;
+  int64_t m, n, k;
+  int accumulate;  // 0: C = A.B^T ; 1: C = C + A.B^T (fp32 add, one rounding)
+};
+
+// CUDA-core FFMA GEMM for any layout (fp32 path, and shapes the tensor-core
+// path does not take).
+cudaError_t launch_gemm_simt(int dtype, const GemmArgs& g, cudaStream_t st);
+
+}  // namespace fljsd

@@ -1,0 +1,409 @@
+// Row kernels of the fused-linear JSD: the three passes over the vocabulary,
+// the valid-row count, the final loss reduction and the backward scaling.
+//
+// The three-pass structure follows "[Perf] Fuse log-softmax into
+// fused_linear_jsd kernel" (Liger-Kernel PR 1352), "Details": pass 1 builds
+// the running max m and denominator d of the student and teacher softmaxes
+// together (online softmax, Milakov & Gimelshein, Algorithm 3); pass 2
+// accumulates the per-row loss and the cross-column term dX_sum; pass 3
+// recomputes dX and writes the logit gradient over the student logits
+// buffer. Logits are read in the input dtype and widened at load; all math is
+// fp32 in registers; e^x is evaluated as 2^(x*log2 e) on the ex2 unit.
+#include "internal.cuh"
+
+#include <math_constants.h>
+
+namespace fljsd {
+namespace {
+
+constexpr int kRowThreads = 512;
+constexpr int kWarps = kRowThreads / 32;
+
+// ---- hardware transcendental units (hand-written PTX) ----------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- vector loads of 16 bytes ------------------------------------------------
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ static void load(const float* p, float (&o)[4]) {
+    float4 v = *reinterpret_cast<const float4*>(p);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+  __device__ static void store(float* p, const float (&o)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
+  }
+  __device__ static float one(const float* p) { return *p; }
+  __device__ static void put(float* p, float x) { *p = x; }
+};
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void load(const __nv_bfloat16* p, float (&o)[8]) {
+    uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, const float (&o)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __device__ static float one(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  __device__ static void put(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+};
+
+// ---- (max, sum of 2^(x - max)) pairs -----------------------------------------
+struct MD {
+  float m, d;
+};
+__device__ __forceinline__ MD md_combine(MD a, MD b) {
+  float m = fmaxf(a.m, b.m);
+  if (m == -CUDART_INF_F) return MD{m, 0.f};
+  float d = (a.m == -CUDART_INF_F ? 0.f : a.d * ex2(a.m - m)) +
+            (b.m == -CUDART_INF_F ? 0.f : b.d * ex2(b.m - m));
+  return MD{m, d};
+}
+
+// Fold a group of values (already in log2 units) into a running (m, d).
+template <int N>
+__device__ __forceinline__ void md_fold(MD& s, const float (&x)[N]) {
+  float vm = x[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) vm = fmaxf(vm, x[i]);
+  if (vm > s.m) {
+    s.d = (s.m == -CUDART_INF_F) ? 0.f : s.d * ex2(s.m - vm);
+    s.m = vm;
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) acc += ex2(x[i] - s.m);
+  s.d += acc;
+}
+
+// Block-wide reductions in a fixed order (deterministic).
+__device__ __forceinline__ MD block_md(MD v, MD* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MD u{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.d, o)};
+    v = md_combine(v, u);
+  }
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  MD r = sh[0];
+  for (int w = 1; w < kWarps; ++w) r = md_combine(r, sh[w]);
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+  }
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  float2 r = sh[0];
+  for (int w = 1; w < kWarps; ++w) {
+    r.x += sh[w].x;
+    r.y += sh[w].y;
+  }
+  __syncthreads();
+  return r;
+}
+
+// ---- per-element branch arithmetic (log2 units) -----------------------------
+// X2 = log2 Q (student), Y2 = log2 P (teacher).
+// BRANCH 0: forward KL(P||Q); 1: reverse KL(Q||P); 2: generalized JSD.
+// Returns the per-element loss (log2 units, i.e. loss / ln 2) and, for the
+// generalized branch, the per-element log-prob gradient dX (also / ln 2).
+template <int BRANCH>
+__device__ __forceinline__ void elem_loss(float X2, float Y2, float beta, float omb,
+                                          float& ell, float& g) {
+  const float Q = ex2(X2), P = ex2(Y2);
+  if (BRANCH == 0) {
+    ell = (X2 == Y2) ? 0.f : P * (Y2 - X2);
+    g = 0.f;
+  } else if (BRANCH == 1) {
+    ell = (X2 == Y2) ? 0.f : Q * (X2 - Y2);
+    g = 0.f;
+  } else {
+    const float M = beta * P + omb * Q;
+    if (X2 == Y2 || M == 0.f) {
+      ell = 0.f;
+      g = 0.f;
+    } else {
+      const float lM = lg2(M);
+      g = omb * Q * (X2 - lM);
+      ell = beta * P * (Y2 - lM) + g;
+    }
+  }
+}
+
+// dlogit of one element, before the row scale w_r / T (natural-log units).
+// L and S are the row loss and dX_sum in log2 units (/ ln 2).
+template <int BRANCH>
+__device__ __forceinline__ float elem_grad(float X2, float Y2, float beta, float omb,
+                                           float L2, float S2) {
+  const float ln2 = 0.6931471805599453f;
+  const float Q = ex2(X2);
+  if (BRANCH == 0) {
+    return Q - ex2(Y2);
+  } else if (BRANCH == 1) {
+    return Q * (ln2 * ((X2 - Y2) - L2));
+  } else {
+    const float P = ex2(Y2);
+    const float M = beta * P + omb * Q;
+    float g = 0.f;
+    if (!(X2 == Y2 || M == 0.f)) g = omb * Q * (X2 - lg2(M));
+    return ln2 * (g - Q * S2);
+  }
+}
+
+template <typename T, int BRANCH>
+__global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
+  using V = Vec<T>;
+  constexpr int N = V::N;
+  __shared__ MD sh_md[kWarps];
+  __shared__ float2 sh_s[kWarps];
+
+  const float c = a.inv_temperature * 1.4426950408889634f;  // log2(e) / T
+  const float beta = a.beta, omb = 1.f - a.beta;
+  const int64_t nvec = a.v / N;
+  const int64_t tail0 = nvec * N;
+  const int n_valid = *a.n_valid;
+
+  for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+    const int64_t grow = a.row0 + r;
+    T* zs = reinterpret_cast<T*>(a.zs) + r * a.ld;
+    const T* zt = reinterpret_cast<const T*>(a.zt) + r * a.ld;
+    const bool valid = (a.labels == nullptr) || (a.labels[grow] != a.ignore_index);
+
+    float w = 0.f;  // row weight w_r
+    if (valid) {
+      switch (a.reduction) {
+        case FLJSD_RED_NONE: w = a.row_grad ? a.row_grad[grow] : 1.f; break;
+        case FLJSD_RED_SUM: w = 1.f; break;
+        case FLJSD_RED_BATCHMEAN: w = n_valid > 0 ? (float)(1.0 / (double)n_valid) : 0.f; break;
+        default: w = n_valid > 0 ? (float)(1.0 / ((double)n_valid * (double)a.v)) : 0.f; break;
+      }
+    }
+    if (!valid) {
+      // ignored row: zero loss and zero gradient over [0, V)
+      float zero[N];
+#pragma unroll
+      for (int i = 0; i < N; ++i) zero[i] = 0.f;
+      for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) V::store(zs + i * N, zero);
+      for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) V::put(zs + j, 0.f);
+      if (threadIdx.x == 0) a.loss_rows[grow] = 0.f;
+      continue;
+    }
+
+    // ---- pass 1: m/d of student (a) and teacher (b) together ----
+    MD ma{-CUDART_INF_F, 0.f}, mb{-CUDART_INF_F, 0.f};
+    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+      float xs[N], xt[N];
+      V::load(zs + i * N, xs);
+      V::load(zt + i * N, xt);
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        xs[k] = __fmul_rn(xs[k], c);
+        xt[k] = __fmul_rn(xt[k], c);
+      }
+      md_fold<N>(ma, xs);
+      md_fold<N>(mb, xt);
+    }
+    for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
+      float xs[1] = {__fmul_rn(V::one(zs + j), c)};
+      float xt[1] = {__fmul_rn(V::one(zt + j), c)};
+      md_fold<1>(ma, xs);
+      md_fold<1>(mb, xt);
+    }
+    const MD ra = block_md(ma, sh_md);
+    const MD rb = block_md(mb, sh_md);
+    const float lse_a = ra.m + lg2(ra.d);  // log2-sum-exp2 of the scaled student logits
+    const float lse_b = rb.m + lg2(rb.d);
+
+    // ---- pass 2: loss and dX_sum ----
+    float2 acc = make_float2(0.f, 0.f);
+    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+      float xs[N], xt[N];
+      V::load(zs + i * N, xs);
+      V::load(zt + i * N, xt);
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        const float X2 = __fsub_rn(__fmul_rn(xs[k], c), lse_a);
+        const float Y2 = __fsub_rn(__fmul_rn(xt[k], c), lse_b);
+        float ell, g;
+        elem_loss<BRANCH>(X2, Y2, beta, omb, ell, g);
+        acc.x += ell;
+        acc.y += g;
+      }
+    }
+    for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
+      const float X2 = __fsub_rn(__fmul_rn(V::one(zs + j), c), lse_a);
+      const float Y2 = __fsub_rn(__fmul_rn(V::one(zt + j), c), lse_b);
+      float ell, g;
+      elem_loss<BRANCH>(X2, Y2, beta, omb, ell, g);
+      acc.x += ell;
+      acc.y += g;
+    }
+    const float2 tot = block_sum2(acc, sh_s);
+    const float L2 = tot.x, S2 = tot.y;  // row loss and dX_sum, / ln 2
+    if (threadIdx.x == 0) a.loss_rows[grow] = 0.6931471805599453f * L2;
+
+    // ---- pass 3: dlogits in place over the student logits ----
+    const float scale = w * a.inv_temperature;
+    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+      float xs[N], xt[N];
+      V::load(zs + i * N, xs);
+      V::load(zt + i * N, xt);
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        const float X2 = __fsub_rn(__fmul_rn(xs[k], c), lse_a);
+        const float Y2 = __fsub_rn(__fmul_rn(xt[k], c), lse_b);
+        xs[k] = elem_grad<BRANCH>(X2, Y2, beta, omb, L2, S2) * scale;
+      }
+      V::store(zs + i * N, xs);
+    }
+    for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
+      const float X2 = __fsub_rn(__fmul_rn(V::one(zs + j), c), lse_a);
+      const float Y2 = __fsub_rn(__fmul_rn(V::one(zt + j), c), lse_b);
+      V::put(zs + j, elem_grad<BRANCH>(X2, Y2, beta, omb, L2, S2) * scale);
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void k_count_valid(const int64_t* labels, int64_t bt, int64_t ignore_index,
+                              int* n_valid) {
+  __shared__ int sh[32];
+  int c = 0;
+  for (int64_t i = threadIdx.x; i < bt; i += blockDim.x)
+    c += (labels == nullptr || labels[i] != ignore_index) ? 1 : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += sh[w];
+    *n_valid = t;
+  }
+}
+
+// Deterministic reduction of the per-row losses: each thread sums a fixed
+// strided subset in double, then a fixed-order tree.
+__global__ void k_reduce_loss(const float* loss_rows, int64_t bt, int64_t v, int reduction,
+                              const int* n_valid, float* loss) {
+  __shared__ double sh[1024];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < bt; i += blockDim.x) s += (double)loss_rows[i];
+  sh[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int n = *n_valid;
+    double r = sh[0];
+    if (n == 0) r = 0.0;
+    else if (reduction == FLJSD_RED_BATCHMEAN) r /= (double)n;
+    else if (reduction == FLJSD_RED_MEAN) r /= (double)n * (double)v;
+    *loss = (float)r;
+  }
+}
+
+template <typename T>
+__global__ void k_scale(T* p, int64_t n, const float* gp) {
+  const float g = *gp;
+  if (g == 1.f) return;
+  using V = Vec<T>;
+  constexpr int N = V::N;
+  const int64_t nvec = n / N;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    float x[N];
+    V::load(p + i * N, x);
+#pragma unroll
+    for (int k = 0; k < N; ++k) x[k] *= g;
+    V::store(p + i * N, x);
+  }
+  for (int64_t j = nvec * N + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n; j += stride)
+    V::put(p + j, V::one(p + j) * g);
+}
+
+template <typename T, int BRANCH>
+cudaError_t launch_rows_t(const JsdRowArgs& a, cudaStream_t st) {
+  const int64_t grid = a.rows < (int64_t)num_sms() * 4 ? a.rows : (int64_t)num_sms() * 4;
+  k_jsd_rows<T, BRANCH><<<(unsigned)grid, kRowThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_rows_dt(const JsdRowArgs& a, cudaStream_t st) {
+  if (a.beta == 0.f) return launch_rows_t<T, 0>(a, st);
+  if (a.beta == 1.f) return launch_rows_t<T, 1>(a, st);
+  return launch_rows_t<T, 2>(a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_jsd_rows(int dtype, const JsdRowArgs& a, cudaStream_t st) {
+  if (a.rows <= 0) return cudaSuccess;
+  trace_begin(FLJSD_KERNEL_JSD_ROWS, st);
+  cudaError_t e = dtype == FLJSD_BF16 ? launch_rows_dt<__nv_bfloat16>(a, st)
+                                      : launch_rows_dt<float>(a, st);
+  trace_end(FLJSD_KERNEL_JSD_ROWS, st);
+  return e;
+}
+
+cudaError_t launch_count_valid(const int64_t* labels, int64_t bt, int64_t ignore_index,
+                               int* n_valid, cudaStream_t st) {
+  trace_begin(FLJSD_KERNEL_SMALL, st);
+  k_count_valid<<<1, 1024, 0, st>>>(labels, bt, ignore_index, n_valid);
+  trace_end(FLJSD_KERNEL_SMALL, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_loss(const float* loss_rows, int64_t bt, int64_t v, int reduction,
+                               const int* n_valid, float* loss, cudaStream_t st) {
+  trace_begin(FLJSD_KERNEL_SMALL, st);
+  k_reduce_loss<<<1, 1024, 0, st>>>(loss_rows, bt, v, reduction, n_valid, loss);
+  trace_end(FLJSD_KERNEL_SMALL, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale(int dtype, void* p, int64_t n, const float* g, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  trace_begin(FLJSD_KERNEL_SMALL, st);
+  const unsigned grid = (unsigned)num_sms() * 4;
+  if (dtype == FLJSD_BF16)
+    k_scale<__nv_bfloat16><<<grid, 256, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(p), n, g);
+  else
+    k_scale<float><<<grid, 256, 0, st>>>(reinterpret_cast<float*>(p), n, g);
+  trace_end(FLJSD_KERNEL_SMALL, st);
+  return cudaGetLastError();
+}
+
+}  // namespace fljsd

@@ -7,6 +7,7 @@ the product library.
 from .fljsd_oracle import (  # noqa: F401
     REDUCTIONS,
     bf16_round,
+    fljsd_from_logits,
     fljsd_ref,
     fljsd_rows_ref,
     jsd_rows,

@@ -198,20 +198,50 @@ def fljsd_ref(x_s, w_s, x_t, w_t, labels=None, *, beta: float = 0.5,
     w_s = np.asarray(w_s, dtype=np.float64)
     x_t = np.asarray(x_t, dtype=np.float64)
     w_t = np.asarray(w_t, dtype=np.float64)
+    bt = x_s.shape[0]
+    v = w_s.shape[0]
+    assert w_s.shape[1] == x_s.shape[1] and x_t.shape[0] == bt and w_t.shape == (v, x_t.shape[1])
+
+    def blocks():
+        for r0 in range(0, bt, block_rows):
+            r1 = min(bt, r0 + block_rows)
+            zs = logits(x_s[r0:r1], w_s)
+            zt = logits(x_t[r0:r1], w_t)
+            if emulate_rounding:
+                zs, zt = bf16_round(zs), bf16_round(zt)
+            yield r0, r1, zs, zt
+
+    return _from_logit_blocks(blocks(), x_s, w_s, labels, beta, temperature, reduction,
+                              ignore_index, row_grad, emulate_rounding)
+
+
+def fljsd_from_logits(z_s, z_t, x_s, w_s, labels=None, *, beta: float = 0.5,
+                      temperature: float = 1.0, reduction: str = "batchmean",
+                      ignore_index: int = -100, row_grad=None, block_rows: int = 256):
+    """The same as ``fljsd_ref`` for logits computed beforehand with ``logits``
+    (so that one pair of logits GEMMs serves a sweep of beta, T and reduction)."""
+    x_s = np.asarray(x_s, dtype=np.float64)
+    w_s = np.asarray(w_s, dtype=np.float64)
+    bt = x_s.shape[0]
+
+    def blocks():
+        for r0 in range(0, bt, block_rows):
+            r1 = min(bt, r0 + block_rows)
+            yield r0, r1, z_s[r0:r1], z_t[r0:r1]
+
+    return _from_logit_blocks(blocks(), x_s, w_s, labels, beta, temperature, reduction,
+                              ignore_index, row_grad, False)
+
+
+def _from_logit_blocks(blocks, x_s, w_s, labels, beta, temperature, reduction, ignore_index,
+                       row_grad, emulate_rounding):
     bt, h_s = x_s.shape
     v = w_s.shape[0]
-    assert w_s.shape == (v, h_s) and x_t.shape[0] == bt and w_t.shape == (v, x_t.shape[1])
     w, valid, n = row_weights(labels, bt, v, reduction, ignore_index, row_grad)
     loss_rows = np.zeros(bt)
     grad_input = np.zeros((bt, h_s))
     grad_weight = np.zeros((v, h_s))
-    for r0 in range(0, bt, block_rows):
-        r1 = min(bt, r0 + block_rows)
-        zs = logits(x_s[r0:r1], w_s)
-        zt = logits(x_t[r0:r1], w_t)
-        if emulate_rounding:
-            zs = bf16_round(zs)
-            zt = bf16_round(zt)
+    for r0, r1, zs, zt in blocks:
         L, dA = jsd_rows(zs, zt, beta, temperature)
         vb = valid[r0:r1]
         L = np.where(vb, L, 0.0)

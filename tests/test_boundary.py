@@ -1,0 +1,147 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point its header declares, plans chunks as documented, and rejects
+bad arguments synchronously with a status before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fljsd.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from lm_head_jsd_gb300.build import build
+
+    build()
+    from lm_head_jsd_gb300 import _lib
+
+    return _lib
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fljsd_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("fljsd_plan", "fljsd_forward", "fljsd_backward", "fljsd_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r"\bT (fljsd_\w+)", out))
+    assert set(_declared_functions()) <= exported
+
+
+def test_status_strings(L):
+    assert L.fljsd_status_string(0) == "ok"
+    assert L.fljsd_status_string(3) == "workspace too small"
+    assert L.fljsd_status_string(99) == "unknown status"
+
+
+def test_plan_single_chunk_and_memory_accounting(L):
+    # PR 1352 "Details", memory table: the two logits tensors take 2*C*V*s bytes
+    # and loss_1d takes BT*4 bytes.
+    p = L.make_problem(8192, 4096, 4096, 128256, "bf16")
+    plan = L.fljsd_plan(p, 0)
+    assert plan.chunk_rows == 8192 and plan.num_chunks == 1 and plan.ld == 128256
+    assert plan.logits_bytes == 2 * 8192 * 128256 * 2
+    assert plan.workspace_bytes >= plan.logits_bytes + 8192 * 4
+    assert plan.workspace_bytes - plan.logits_bytes < 64 * 1024 + 8192 * 4 * 2
+    # ld is padded to a multiple of 8 elements (16-byte rows in bf16)
+    plan = L.fljsd_plan(L.make_problem(64, 128, 128, 1000, "fp32"), 0)
+    assert plan.ld == 1000
+    plan = L.fljsd_plan(L.make_problem(64, 128, 128, 1001, "bf16"), 0)
+    assert plan.ld == 1008 and plan.logits_bytes == 2 * 64 * 1008 * 2
+
+
+def test_planner_fits_free_memory(L):
+    p = L.make_problem(8192, 4096, 4096, 128256, "bf16")
+    one_chunk = L.fljsd_plan(p, 0).workspace_bytes
+    plan = L.fljsd_plan(p, one_chunk)  # only half of it may be used
+    assert plan.chunk_rows % 128 == 0 and 0 < plan.chunk_rows < 8192
+    assert plan.workspace_bytes <= one_chunk // 2
+    assert plan.num_chunks == -(-8192 // plan.chunk_rows)
+    bigger = L.fljsd_plan(p, 4 * one_chunk)
+    assert bigger.chunk_rows == 8192
+    # explicit chunk rows are honoured and clamped to bt
+    p.chunk_rows = 512
+    assert L.fljsd_plan(p, 0).chunk_rows == 512
+    p.chunk_rows = 100000
+    assert L.fljsd_plan(p, 0).chunk_rows == 8192
+    # not even one row fits
+    p.chunk_rows = 0
+    with pytest.raises(L.FljsdError) as e:
+        L.fljsd_plan(p, 1024)
+    assert e.value.status == 3
+
+
+@pytest.mark.parametrize("field,value", [
+    ("bt", 0), ("h_s", -1), ("h_t", 0), ("v", 0), ("dtype", 7), ("reduction", 9),
+    ("beta", 1.5), ("beta", -0.1), ("beta", float("nan")), ("temperature", 0.0),
+    ("temperature", -1.0), ("temperature", float("inf")), ("temperature", float("nan")),
+    ("chunk_rows", -4),
+])
+def test_plan_rejects_bad_problems(L, field, value):
+    p = L.make_problem(16, 32, 32, 100, "bf16")
+    setattr(p, field, value)
+    with pytest.raises(L.FljsdError) as e:
+        L.fljsd_plan(p, 0)
+    assert e.value.status == 1
+
+
+def _fake(addr=1 << 20):
+    return addr  # an aligned, never dereferenced address
+
+
+def test_forward_argument_checks_need_no_device(L):
+    p = L.make_problem(16, 32, 32, 100, "bf16")
+    plan = L.fljsd_plan(p, 0)
+    good = dict(x_s=_fake(), w_s=_fake(), x_t=_fake(), w_t=_fake(), labels=None, row_grad=None,
+                loss=_fake(), grad_input=_fake(), grad_weight=_fake(), workspace=_fake())
+
+    def call(ws_bytes=plan.workspace_bytes, problem=p, pl=plan, **over):
+        a = dict(good, **over)
+        return L.fljsd_forward(problem, pl, a["x_s"], a["w_s"], a["x_t"], a["w_t"], a["labels"],
+                               a["row_grad"], a["loss"], a["grad_input"], a["grad_weight"],
+                               a["workspace"], workspace_bytes=ws_bytes, stream=0, check=False)
+
+    for k in ("x_s", "w_s", "x_t", "w_t", "loss", "grad_input", "grad_weight", "workspace"):
+        assert call(**{k: None}) == 1, k
+        assert call(**{k: _fake() + 8}) == 1, k  # misaligned
+    assert call(labels=_fake() + 4) == 1
+    assert call(ws_bytes=plan.workspace_bytes - 1) == 3
+    other = L.fljsd_plan(L.make_problem(16, 32, 32, 200, "bf16"), 0)
+    assert call(pl=other) == 1  # plan made for another problem
+    bad = L.make_problem(16, 32, 32, 100, "bf16", beta=2.0)
+    assert call(problem=bad) == 1
+
+
+def test_backward_argument_checks_need_no_device(L):
+    p = L.make_problem(16, 32, 32, 100, "bf16")
+    assert L.fljsd_backward(p, None, _fake(), _fake(), stream=0, check=False) == 1
+    assert L.fljsd_backward(p, _fake(), None, _fake(), stream=0, check=False) == 1
+    assert L.fljsd_backward(p, _fake(), _fake() + 2, _fake(), stream=0, check=False) == 1
+
+
+def test_package_has_no_cpu_fallback():
+    """The product package never imports the oracle, and nothing in it computes
+    the loss with torch: every step runs in libfljsd.so."""
+    pkg = os.path.join(ROOT, "lm_head_jsd_gb300")
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            src = open(os.path.join(pkg, fn)).read()
+            assert "oracle" not in src, fn
+            for forbidden in ("log_softmax", "torch.matmul", "softmax(", " @ "):
+                assert forbidden not in src, (fn, forbidden)

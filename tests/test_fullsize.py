@@ -1,0 +1,99 @@
+"""GPU parity at the full workload sizes (V=128256, BT up to 8192).
+
+The oracle cannot afford every row here, so the checks use outputs it can
+compute one row at a time, plus properties that hold at any size:
+
+A. the benchmarked launch (the workload's reduction, labels and chunking):
+   sampled grad_input rows against the oracle's rows, ignored rows exactly 0,
+   and the identity <grad_weight, W_s> == <grad_input, X_s> (both equal
+   <dZ, Z_s>);
+B. reduction "none": the sampled per-row losses against the oracle, and the
+   scalar loss of A equal to their reduction;
+C. every row ignored except the sampled ones: then grad_weight is a sum over
+   the sampled rows only, and the whole V x H matrix is compared element by
+   element with the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import jsd_inputs
+import oracle
+from parity_util import TOL, assert_zeros_where_ref_zero, f64, rel_fro, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+CASES = [("llama3_lmhead", 4096), ("llama3_lmhead", 512), ("llama3_lmhead", 128),
+         ("large_teacher", 0), ("headline", 0)]
+N_SAMPLE = 24
+
+
+@pytest.mark.parametrize("name,chunk", CASES, ids=[f"{n}-c{c}" for n, c in CASES])
+def test_full_size(name, chunk):
+    w = jsd_inputs.WORKLOADS[name]
+    dev = "cuda:0"
+    x_s, w_s, x_t, w_t, labels = jsd_inputs.make_inputs(w, dev)
+    tol_loss, tol_grad = TOL[w.dtype]
+    kw = dict(beta=w.beta, temperature=w.temperature, chunk_rows=chunk)
+
+    g = torch.Generator().manual_seed(1000 + w.seed)
+    R = torch.randperm(w.bt, generator=g)[:N_SAMPLE].sort().values
+    lab_cpu = None if labels is None else labels.cpu()
+    valid = np.ones(w.bt, bool) if lab_cpu is None else (lab_cpu.numpy() != -100)
+    n = int(valid.sum())
+
+    xs64, xt64 = f64(x_s[R.to(dev)]), f64(x_t[R.to(dev)])
+    ws64, wt64 = f64(w_s), f64(w_t)
+    # per-row oracle for the sampled rows with weight 1 (sum)
+    L_ref, dz1, gi1 = oracle.fljsd_rows_ref(xs64, ws64, xt64, wt64, beta=w.beta,
+                                            temperature=w.temperature,
+                                            row_scale=np.ones(N_SAMPLE))
+    vR = valid[R.numpy()]
+    L_ref = np.where(vR, L_ref, 0.0)
+    gi1[~vR] = 0.0
+    dz1[~vR] = 0.0
+
+    # ---- A: the benchmarked launch ----
+    lossA, giA, gwA = run_gpu(x_s, w_s, x_t, w_t, labels, reduction=w.reduction, **kw)
+    scale = {"batchmean": 1.0 / n, "sum": 1.0, "mean": 1.0 / (n * w.v)}[w.reduction]
+    giA_R = f64(giA[R.to(dev)])
+    e = rel_fro(giA_R, scale * gi1)
+    assert e <= tol_grad, f"A grad_input sampled rows: {e:.3g}"
+    assert_zeros_where_ref_zero(giA_R, scale * gi1, "A grad_input rows")
+    ign = np.nonzero(~valid)[0]
+    if len(ign):
+        assert int(torch.count_nonzero(giA[torch.from_numpy(ign).to(dev)])) == 0
+    lhs = torch.sum(gwA.double() * w_s.double()).item()
+    rhs = torch.sum(giA.double() * x_s.double()).item()
+    bound = (torch.linalg.vector_norm(gwA.double()) * torch.linalg.vector_norm(w_s.double())).item()
+    assert abs(lhs - rhs) <= 2e-3 * bound, (lhs, rhs, bound)
+    assert torch.all(torch.isfinite(gwA.float())) and torch.all(torch.isfinite(giA.float()))
+    del giA, gwA
+    torch.cuda.empty_cache()
+
+    # ---- B: per-row losses ----
+    lossB, giB, gwB = run_gpu(x_s, w_s, x_t, w_t, labels, reduction="none", **kw)
+    LB = f64(lossB)
+    e = rel_fro(LB[R.numpy()], L_ref)
+    assert e <= tol_loss, f"B sampled row losses: {e:.3g}"
+    assert np.all(LB[~valid] == 0.0)
+    assert abs(lossA.item() - LB.sum() * scale) <= 1e-5 * abs(LB.sum() * scale)
+    del giB, gwB
+    torch.cuda.empty_cache()
+
+    # ---- C: only the sampled rows count; grad_weight compared in full ----
+    labC = torch.full((w.bt,), -100, dtype=torch.int64)
+    labC[R] = 0
+    labC[R[~torch.from_numpy(vR)]] = -100
+    lossC, giC, gwC = run_gpu(x_s, w_s, x_t, w_t, labC, reduction="sum", **kw)
+    assert abs(lossC.item() - L_ref.sum()) <= tol_loss * abs(L_ref.sum())
+    gw_ref = dz1.T @ xs64
+    gwC64 = f64(gwC)
+    e = rel_fro(gwC64, gw_ref)
+    assert e <= tol_grad, f"C grad_weight: {e:.3g}"
+    assert_zeros_where_ref_zero(gwC64, gw_ref, "C grad_weight")
+    e = rel_fro(f64(giC[R.to(dev)]), gi1)
+    assert e <= tol_grad, f"C grad_input rows: {e:.3g}"
+    mask = torch.ones(w.bt, dtype=torch.bool)
+    mask[R] = False
+    assert int(torch.count_nonzero(giC[mask.to(dev)])) == 0

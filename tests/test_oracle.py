@@ -332,3 +332,18 @@ def test_row_weights_reading():
     w, valid, n = row_weights(np.array([1, -100, 2]), 3, 10, "mean")
     assert n == 2 and list(valid) == [True, False, True]
     np.testing.assert_allclose(w, [1 / 20, 0, 1 / 20])
+
+
+def test_from_logits_matches_full_reference():
+    from oracle import fljsd_from_logits, logits
+
+    x_s, w_s, x_t, w_t = _problem(17, bt=9, h=5, v=21)
+    labels = np.array([0, 1, -100, 3, 4, 5, -100, 7, 8])
+    zs, zt = logits(x_s, w_s), logits(x_t, w_t)
+    for red in ("none", "mean"):
+        a = fljsd_ref(x_s, w_s, x_t, w_t, labels, beta=0.3, temperature=1.5, reduction=red)
+        b = fljsd_from_logits(zs, zt, x_s, w_s, labels, beta=0.3, temperature=1.5, reduction=red,
+                              block_rows=4)
+        np.testing.assert_allclose(a[0], b[0], rtol=1e-13)
+        np.testing.assert_allclose(a[1], b[1], rtol=1e-12)
+        np.testing.assert_allclose(a[2], b[2], rtol=1e-11, atol=1e-16)

@@ -1,0 +1,218 @@
+"""GPU parity: the CUDA library against the float64 CPU oracle on the same seeded
+inputs, element by element, with the stated tolerances (loss relative error
+<= 1e-5 fp32 / 2e-3 bf16; gradient relative Frobenius error <= 1e-5 fp32 /
+1e-2 bf16; exactly 0.0 wherever the oracle is exactly 0)."""
+import numpy as np
+import pytest
+import torch
+
+import jsd_inputs
+import oracle
+from parity_util import TOL, compare, f64, rel_fro, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+BETAS = (0.0, 0.1, 0.5, 1.0)
+REDS = ("none", "sum", "mean", "batchmean")
+
+
+def _oracle(inputs, **kw):
+    x_s, w_s, x_t, w_t, labels = inputs
+    return oracle.fljsd_ref(f64(x_s), f64(w_s), f64(x_t), f64(w_t), f64(labels), **kw)
+
+
+# ---------------------------------------------------------------------------
+# tiny fp32: every branch, temperature and reduction
+# ---------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def tiny():
+    return jsd_inputs.make_inputs(jsd_inputs.WORKLOADS["tiny_fp32"], "cpu")
+
+
+@pytest.mark.parametrize("beta", BETAS)
+@pytest.mark.parametrize("T", [1.0, 2.0])
+@pytest.mark.parametrize("red", REDS)
+def test_tiny_fp32(tiny, beta, T, red):
+    out = run_gpu(*tiny, beta=beta, temperature=T, reduction=red)
+    ref = _oracle(tiny, beta=beta, temperature=T, reduction=red)
+    compare(out, ref, "fp32", f"tiny beta={beta} T={T} {red}")
+
+
+# ---------------------------------------------------------------------------
+# ties: self-distillation gives exact zeros; padded vocabulary
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("copies", [False, True])
+@pytest.mark.parametrize("beta", BETAS)
+def test_self_distillation_exact_zeros(beta, copies):
+    w = jsd_inputs.WORKLOADS["ties_self"]
+    x_s, w_s, x_t, w_t, labels = jsd_inputs.make_inputs(w, "cuda:0")
+    if copies:
+        x_t, w_t = x_s.clone(), w_s.clone()
+    loss, gi, gw = run_gpu(x_s, w_s, x_t, w_t, labels, beta=beta, temperature=w.temperature,
+                           reduction=w.reduction)
+    assert loss.item() == 0.0
+    assert int(torch.count_nonzero(gi)) == 0 and int(torch.count_nonzero(gw)) == 0
+
+
+def test_padded_vocab():
+    w = jsd_inputs.WORKLOADS["ties_padded"]
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    out = run_gpu(*inputs, beta=w.beta, temperature=w.temperature, reduction=w.reduction)
+    ref = _oracle(inputs, beta=w.beta, temperature=w.temperature, reduction=w.reduction)
+    compare(out, ref, "bf16", "padded vocab")
+
+
+# ---------------------------------------------------------------------------
+# multi-block vocabulary with a partial trailing block: the full sweep
+# ---------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def multiblock():
+    w = jsd_inputs.WORKLOADS["multiblock"]
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    x_s, w_s, x_t, w_t, labels = (f64(t) for t in inputs)
+    zs = oracle.logits(x_s, w_s)
+    zt = oracle.logits(x_t, w_t)
+    return inputs, (zs, zt, x_s, w_s, labels)
+
+
+@pytest.mark.parametrize("beta", (0.0, 0.5, 1.0))
+@pytest.mark.parametrize("T", (1.0, 2.0))
+@pytest.mark.parametrize("red", REDS)
+def test_multiblock_sweep(multiblock, beta, T, red):
+    inputs, (zs, zt, x_s, w_s, labels) = multiblock
+    out = run_gpu(*inputs, beta=beta, temperature=T, reduction=red)
+    ref = oracle.fljsd_from_logits(zs, zt, x_s, w_s, labels, beta=beta, temperature=T,
+                                   reduction=red)
+    compare(out, ref, "bf16", f"multiblock beta={beta} T={T} {red}")
+
+
+# ---------------------------------------------------------------------------
+# small and ragged shapes, chunking, upstream gradients
+# ---------------------------------------------------------------------------
+SMALL = [
+    # (bt, h, v, dtype)
+    (1, 8, 1, "bf16"), (1, 8, 7, "bf16"), (3, 16, 33, "bf16"), (130, 24, 1000, "bf16"),
+    (257, 72, 4099, "bf16"), (1, 5, 1, "fp32"), (2, 7, 13, "fp32"), (65, 17, 1001, "fp32"),
+    (129, 64, 9000, "bf16"),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("beta", (0.0, 0.3, 1.0))
+def test_small_shapes(shape, beta):
+    bt, h, v, dt = shape
+    w = jsd_inputs.custom("small", 11 + bt + v, bt, h, v, dt, ignore_frac=0.25 if bt >= 4 else 0.0)
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    for red in ("none", "batchmean"):
+        out = run_gpu(*inputs, beta=beta, temperature=1.3, reduction=red)
+        ref = _oracle(inputs, beta=beta, temperature=1.3, reduction=red)
+        compare(out, ref, dt, f"{shape} beta={beta} {red}")
+
+
+@pytest.mark.parametrize("chunk", [1, 7, 64, 128, 300])
+def test_chunking_accumulates_grad_weight(chunk):
+    w = jsd_inputs.custom("chunks", 21, 300, 64, 5000, "bf16", ignore_frac=0.1)
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    out = run_gpu(*inputs, beta=0.5, temperature=1.0, reduction="batchmean", chunk_rows=chunk)
+    ref = _oracle(inputs, beta=0.5, temperature=1.0, reduction="batchmean")
+    compare(out, ref, "bf16", f"chunk={chunk}")
+    out32 = run_gpu(*(t.float() if t is not None and t.is_floating_point() else t for t in inputs),
+                    beta=0.5, reduction="batchmean", chunk_rows=chunk)
+    compare(out32, ref, "fp32", f"fp32 chunk={chunk}")
+
+
+def test_row_grad_with_reduction_none():
+    w = jsd_inputs.custom("rowgrad", 31, 40, 32, 700, "fp32", ignore_frac=0.2)
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    rg = torch.linspace(-1.0, 2.0, 40)
+    out = run_gpu(*inputs, beta=0.2, temperature=2.0, reduction="none", row_grad=rg)
+    ref = _oracle(inputs, beta=0.2, temperature=2.0, reduction="none", row_grad=rg.numpy())
+    compare(out, ref, "fp32", "row_grad")
+
+
+def test_all_rows_ignored():
+    w = jsd_inputs.custom("allign", 32, 16, 32, 300, "bf16")
+    x_s, w_s, x_t, w_t, _ = jsd_inputs.make_inputs(w, "cpu")
+    labels = torch.full((16,), -100, dtype=torch.int64)
+    for red in REDS:
+        loss, gi, gw = run_gpu(x_s, w_s, x_t, w_t, labels, reduction=red)
+        assert torch.all(loss == 0) and torch.count_nonzero(gi) == 0
+        assert torch.count_nonzero(gw) == 0
+
+
+def test_backward_scales_by_grad_output():
+    from lm_head_jsd_gb300 import FusedLinearJSD
+
+    w = jsd_inputs.custom("bwd", 33, 64, 32, 500, "fp32")
+    x_s, w_s, x_t, w_t, _ = (t.cuda() if t is not None else None
+                             for t in jsd_inputs.make_inputs(w, "cpu"))
+    run = FusedLinearJSD(64, 32, 32, 500, torch.float32)
+    loss, gi, gw = run.forward(x_s, w_s, x_t, w_t)
+    gi0, gw0 = gi.clone(), gw.clone()
+    run.backward(torch.ones(1, device="cuda"), gi, gw)
+    assert torch.equal(gi, gi0) and torch.equal(gw, gw0)
+    run.backward(torch.full((1,), -2.5, device="cuda"), gi, gw)
+    torch.testing.assert_close(gi, gi0 * -2.5, rtol=1e-6, atol=0)
+    torch.testing.assert_close(gw, gw0 * -2.5, rtol=1e-6, atol=0)
+
+
+def test_autograd_function():
+    from lm_head_jsd_gb300 import fused_linear_jsd
+
+    w = jsd_inputs.custom("autograd", 34, 48, 32, 600, "fp32", ignore_frac=0.1)
+    x_s, w_s, x_t, w_t, labels = jsd_inputs.make_inputs(w, "cpu")
+    xs = x_s.cuda().requires_grad_(True)
+    ws = w_s.cuda().requires_grad_(True)
+    loss = fused_linear_jsd(xs, ws, x_t.cuda(), w_t.cuda(), labels.cuda(), beta=0.4,
+                            temperature=1.5, reduction="sum")
+    (3.0 * loss).backward()
+    ref = oracle.fljsd_ref(f64(x_s), f64(w_s), f64(x_t), f64(w_t), f64(labels), beta=0.4,
+                           temperature=1.5, reduction="sum")
+    assert abs(loss.item() - ref[0]) / abs(ref[0]) <= 1e-5
+    assert rel_fro(f64(xs.grad), 3.0 * ref[1]) <= 1e-5
+    assert rel_fro(f64(ws.grad), 3.0 * ref[2]) <= 1e-5
+    # reduction="none" with a non-uniform upstream gradient
+    xs.grad = None
+    ws.grad = None
+    rows = fused_linear_jsd(xs, ws, x_t.cuda(), w_t.cuda(), labels.cuda(), beta=0.4,
+                            temperature=1.5, reduction="none")
+    up = torch.linspace(0.5, 1.5, 48, device="cuda")
+    (rows * up).sum().backward()
+    ref = oracle.fljsd_ref(f64(x_s), f64(w_s), f64(x_t), f64(w_t), f64(labels), beta=0.4,
+                           temperature=1.5, reduction="none", row_grad=f64(up))
+    assert rel_fro(f64(xs.grad), ref[1]) <= 1e-5
+    assert rel_fro(f64(ws.grad), ref[2]) <= 1e-5
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Guard bands: outputs are views into larger buffers filled with a canary;
+    nothing outside the views may change, and every element inside is written."""
+    from lm_head_jsd_gb300 import FusedLinearJSD
+
+    w = jsd_inputs.custom("guard", 35, 77, 40, 1234, "bf16", ignore_frac=0.1)
+    x_s, w_s, x_t, w_t, labels = (t.cuda() for t in jsd_inputs.make_inputs(w, "cpu"))
+    run = FusedLinearJSD(77, 40, 40, 1234, torch.bfloat16, reduction="none", chunk_rows=32)
+    pad = 4096
+    canary = 12345.0
+
+    def guarded(n, dt):
+        buf = torch.full((n + 2 * pad,), canary, dtype=dt, device="cuda")
+        return buf, buf[pad:pad + n]
+
+    lb, loss = guarded(77, torch.float32)
+    gib, gi = guarded(77 * 40, torch.bfloat16)
+    gwb, gw = guarded(1234 * 40, torch.bfloat16)
+    run.forward(x_s, w_s, x_t, w_t, labels, out=(loss, gi.view(77, 40), gw.view(1234, 40)))
+    torch.cuda.synchronize()
+    for buf, n in ((lb, 77), (gib, 77 * 40), (gwb, 1234 * 40)):
+        assert torch.all(buf[:pad] == canary) and torch.all(buf[pad + n:] == canary)
+        assert not torch.any(buf[pad:pad + n] == canary)
+
+
+def test_deterministic():
+    w = jsd_inputs.custom("det", 36, 200, 64, 3000, "bf16", ignore_frac=0.1)
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    a = run_gpu(*inputs, beta=0.5)
+    b = run_gpu(*inputs, beta=0.5)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
