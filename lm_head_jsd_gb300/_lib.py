@@ -45,7 +45,7 @@ class fljsd_plan_t(ctypes.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python -m lm_head_jsd_gb300.build` (there is no CPU fallback)")
+                          "`python lm_head_jsd_gb300/build.py` (there is no CPU fallback)")
     lib = ctypes.CDLL(LIB_PATH)
     P = ctypes.c_void_p
     lib.fljsd_plan.argtypes = [ctypes.POINTER(fljsd_problem), ctypes.c_size_t,

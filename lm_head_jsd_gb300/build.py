@@ -1,7 +1,9 @@
 """Build libfljsd.so in-tree with nvcc for sm_103a.
 
-    python -m lm_head_jsd_gb300.build          # build if any source is newer
-    python -m lm_head_jsd_gb300.build --force  # rebuild everything
+    python lm_head_jsd_gb300/build.py          # build if any source is newer
+    python lm_head_jsd_gb300/build.py --force  # rebuild everything
+
+It imports nothing from the package (whose import loads the library).
 
 Each CUDA source is compiled to an object in parallel under ``_build/`` at the
 repository root, then linked into ``lm_head_jsd_gb300/libfljsd.so`` with the

@@ -20,3 +20,10 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.fail("gpu test collected but no CUDA device is visible")
     return torch.device("cuda:0")
+
+
+def build_library():
+    """Build libfljsd.so if needed (through the build script, loaded by path)."""
+    import __graft_entry__
+
+    __graft_entry__.build()

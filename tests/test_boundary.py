@@ -14,9 +14,9 @@ HEADER = os.path.join(ROOT, "include", "fljsd.h")
 
 @pytest.fixture(scope="module")
 def L():
-    from lm_head_jsd_gb300.build import build
+    from conftest import build_library
 
-    build()
+    build_library()
     from lm_head_jsd_gb300 import _lib
 
     return _lib
