@@ -98,6 +98,7 @@ typedef struct {
   size_t workspace_bytes; /* device bytes fljsd_forward needs */
   size_t logits_bytes;    /* 2 * C * ld * sizeof(dtype): the two logits buffers */
   size_t stats_bytes;     /* per-row and per-tile statistics */
+  size_t status_offset;   /* byte offset of the int32 device status word in the workspace */
 } fljsd_plan_t;
 
 /*
@@ -151,6 +152,34 @@ fljsd_status fljsd_forward(const fljsd_problem* problem, const fljsd_plan_t* pla
  */
 fljsd_status fljsd_backward(const fljsd_problem* problem, const float* grad_output,
                             void* grad_input, void* grad_weight, fljsd_stream_t stream);
+
+/*
+ * fljsd_workspace_status -- the device status word of the last fljsd_forward
+ * that used `workspace` (FLJSD_OK, or FLJSD_ERR_TIMEOUT if a bounded wait
+ * inside a kernel expired). Synchronises `stream`, then copies 4 bytes to
+ * the host into *device_status. Returns FLJSD_ERR_CUDA if the copy fails.
+ */
+fljsd_status fljsd_workspace_status(const fljsd_plan_t* plan, const void* workspace,
+                                    fljsd_stream_t stream, int32_t* device_status);
+
+/*
+ * fljsd_gemm_bf16 -- the tensor-core contraction used by the path, exposed
+ * as a building block: D[m x n] = A . B^T (accumulate == 0) or
+ * D = D + A . B^T (accumulate == 1; the stored value and the fp32 product
+ * are added and rounded once, as for grad_weight in PR 1429, "Summary").
+ *   a_mn == 0: A stored [m x k] row-major with row stride lda (k contiguous);
+ *   a_mn == 1: A stored [k x m] row-major with row stride lda (m contiguous);
+ *   b_mn == 0: B stored [n x k]; b_mn == 1: B stored [k x n] (stride ldb);
+ *   D stored [m x ldd]. All bf16, device, 16-byte aligned; lda, ldb, ldd
+ *   multiples of 8; m, n, k >= 1.
+ * status: device int32 that receives FLJSD_ERR_TIMEOUT if a bounded wait
+ * expires (may be NULL). Asynchronous on `stream`. FLJSD_ERR_INVALID_ARG for
+ * shapes or alignments outside the above.
+ */
+fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const void* b,
+                             int64_t ldb, int32_t b_mn, void* d, int64_t ldd, int64_t m,
+                             int64_t n, int64_t k, int32_t accumulate, int32_t* status,
+                             fljsd_stream_t stream);
 
 /* Static, human-readable name of a status code. Never NULL. */
 const char* fljsd_status_string(fljsd_status status);

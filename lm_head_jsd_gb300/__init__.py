@@ -8,6 +8,7 @@ from ._lib import (  # noqa: F401
     FljsdError,
     fljsd_backward,
     fljsd_forward,
+    fljsd_gemm_bf16,
     fljsd_launch_count,
     fljsd_launch_count_reset,
     fljsd_plan,
@@ -15,6 +16,7 @@ from ._lib import (  # noqa: F401
     fljsd_trace_enable,
     fljsd_trace_read,
     fljsd_trace_reset,
+    fljsd_workspace_status,
     make_problem,
 )
 from .api import FusedLinearJSD, fused_linear_jsd  # noqa: F401

@@ -39,7 +39,8 @@ class fljsd_problem(ctypes.Structure):
 class fljsd_plan_t(ctypes.Structure):
     _fields_ = [("chunk_rows", ctypes.c_int64), ("num_chunks", ctypes.c_int64),
                 ("ld", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t),
-                ("logits_bytes", ctypes.c_size_t), ("stats_bytes", ctypes.c_size_t)]
+                ("logits_bytes", ctypes.c_size_t), ("stats_bytes", ctypes.c_size_t),
+                ("status_offset", ctypes.c_size_t)]
 
 
 def _load():
@@ -56,6 +57,13 @@ def _load():
     lib.fljsd_forward.restype = ctypes.c_int
     lib.fljsd_backward.argtypes = [ctypes.POINTER(fljsd_problem), P, P, P, P]
     lib.fljsd_backward.restype = ctypes.c_int
+    lib.fljsd_workspace_status.argtypes = [ctypes.POINTER(fljsd_plan_t), P, P,
+                                           ctypes.POINTER(ctypes.c_int32)]
+    lib.fljsd_workspace_status.restype = ctypes.c_int
+    lib.fljsd_gemm_bf16.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, ctypes.c_int64,
+                                    ctypes.c_int32, P, ctypes.c_int64, ctypes.c_int64,
+                                    ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, P, P]
+    lib.fljsd_gemm_bf16.restype = ctypes.c_int
     lib.fljsd_status_string.argtypes = [ctypes.c_int]
     lib.fljsd_status_string.restype = ctypes.c_char_p
     lib.fljsd_launch_count.argtypes = []
@@ -132,6 +140,24 @@ def fljsd_backward(problem, grad_output, grad_input, grad_weight, stream=None,
                             _ptr(grad_weight), _stream(stream))
     if check and st != FLJSD_OK:
         raise FljsdError(st, "fljsd_backward")
+    return st
+
+
+def fljsd_workspace_status(plan, workspace, stream=None) -> int:
+    out = ctypes.c_int32()
+    st = lib.fljsd_workspace_status(ctypes.byref(plan), _ptr(workspace), _stream(stream),
+                                    ctypes.byref(out))
+    if st != FLJSD_OK:
+        raise FljsdError(st, "fljsd_workspace_status")
+    return out.value
+
+
+def fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate=0, status=None,
+                    stream=None, check=True) -> int:
+    st = lib.fljsd_gemm_bf16(_ptr(a), lda, a_mn, _ptr(b), ldb, b_mn, _ptr(d), ldd, m, n, k,
+                             accumulate, _ptr(status), _stream(stream))
+    if check and st != FLJSD_OK:
+        raise FljsdError(st, "fljsd_gemm_bf16")
     return st
 
 

@@ -3,6 +3,7 @@
 // accounting and per-kernel event timing. Declarations and semantics are in
 // include/fljsd.h.
 #include "internal.cuh"
+#include "gemm_tc.cuh"
 
 #include <atomic>
 #include <cmath>
@@ -116,6 +117,31 @@ fljsd_status check_problem(const fljsd_problem* p) {
 
 inline bool aligned16(const void* q) { return ((uintptr_t)q & 15u) == 0; }
 
+// One contraction D (+)= A . B^T of the path. Operand storage as in
+// TcGemmArgs: a_mn / b_mn select an operand stored with the contraction
+// dimension as its outer (row) dimension. bf16 goes to the tensor cores
+// whenever the strides allow TMA (multiples of 8 elements); fp32 and the
+// remaining bf16 shapes use the CUDA-core kernel.
+cudaError_t run_gemm(int dtype, int kind, const void* a, int64_t lda, int a_mn, const void* b,
+                     int64_t ldb, int b_mn, void* d, int64_t ldd, int64_t m, int64_t n, int64_t k,
+                     int accumulate, int raster_n_fastest, int* status, cudaStream_t st) {
+  if (m <= 0 || n <= 0) return cudaSuccess;
+  cudaError_t e;
+  trace_begin(kind, st);
+  TcGemmArgs t{a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, raster_n_fastest, status};
+  if (dtype == FLJSD_BF16 && tc_gemm_supported(t)) {
+    e = launch_gemm_tc(t, st);
+  } else {
+    GemmArgs g{};
+    g.a = a; g.sam = a_mn ? 1 : lda; g.sak = a_mn ? lda : 1;
+    g.b = b; g.sbn = b_mn ? 1 : ldb; g.sbk = b_mn ? ldb : 1;
+    g.c = d; g.ldc = ldd; g.m = m; g.n = n; g.k = k; g.accumulate = accumulate;
+    e = launch_gemm_simt(dtype, g, st);
+  }
+  trace_end(kind, st);
+  return e;
+}
+
 }  // namespace
 }  // namespace fljsd
 
@@ -167,6 +193,7 @@ fljsd_status fljsd_plan(const fljsd_problem* p, size_t free_hbm_bytes, fljsd_pla
   out->workspace_bytes = L.total;
   out->logits_bytes = L.logits_bytes;
   out->stats_bytes = L.stats_bytes;
+  out->status_offset = L.misc + sizeof(int);
   return FLJSD_OK;
 }
 
@@ -200,6 +227,7 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
   void* zt = ws + L.zt;
   float* loss_rows = p->reduction == FLJSD_RED_NONE ? loss : reinterpret_cast<float*>(ws + L.loss_rows);
   int* n_valid = reinterpret_cast<int*>(ws + L.misc);
+  int* status = n_valid + 1;  // device status word, reset by the row-count kernel
   const size_t s = dtype_size(p->dtype);
 
   cudaError_t e = launch_count_valid(labels, p->bt, p->ignore_index, n_valid, stream);
@@ -211,21 +239,12 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
     const char* xs_c = static_cast<const char*>(x_s) + (size_t)r0 * p->h_s * s;
     const char* xt_c = static_cast<const char*>(x_t) + (size_t)r0 * p->h_t * s;
 
-    // student and teacher logits, rounded to the input dtype
-    GemmArgs g{};
-    g.a = xs_c; g.sam = p->h_s; g.sak = 1;
-    g.b = w_s; g.sbn = p->h_s; g.sbk = 1;
-    g.c = zs; g.ldc = L.ld; g.m = rows; g.n = p->v; g.k = p->h_s; g.accumulate = 0;
-    trace_begin(FLJSD_KERNEL_GEMM_LOGITS, stream);
-    e = launch_gemm_simt(p->dtype, g, stream);
-    trace_end(FLJSD_KERNEL_GEMM_LOGITS, stream);
+    // student and teacher logits, rounded to the input dtype (X . W^T, both K-major)
+    e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_LOGITS, xs_c, p->h_s, 0, w_s, p->h_s, 0, zs, L.ld,
+                 rows, p->v, p->h_s, 0, 0, status, stream);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
-    g.a = xt_c; g.sam = p->h_t;
-    g.b = w_t; g.sbn = p->h_t;
-    g.c = zt; g.k = p->h_t;
-    trace_begin(FLJSD_KERNEL_GEMM_LOGITS, stream);
-    e = launch_gemm_simt(p->dtype, g, stream);
-    trace_end(FLJSD_KERNEL_GEMM_LOGITS, stream);
+    e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_LOGITS, xt_c, p->h_t, 0, w_t, p->h_t, 0, zt, L.ld,
+                 rows, p->v, p->h_t, 0, 0, status, stream);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
     // three passes over V; dlogits overwrite the student logits
@@ -238,26 +257,16 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
     e = launch_jsd_rows(p->dtype, ra, stream);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
-    // grad_input rows of this chunk = dZ . W_s
-    GemmArgs gi{};
-    gi.a = zs; gi.sam = L.ld; gi.sak = 1;
-    gi.b = w_s; gi.sbn = 1; gi.sbk = p->h_s;
-    gi.c = static_cast<char*>(grad_input) + (size_t)r0 * p->h_s * s; gi.ldc = p->h_s;
-    gi.m = rows; gi.n = p->h_s; gi.k = p->v; gi.accumulate = 0;
-    trace_begin(FLJSD_KERNEL_GEMM_GRAD_INPUT, stream);
-    e = launch_gemm_simt(p->dtype, gi, stream);
-    trace_end(FLJSD_KERNEL_GEMM_GRAD_INPUT, stream);
+    // grad_input rows of this chunk = dZ . W_s (W_s stored [V x H]: B is N-major)
+    e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_INPUT, zs, L.ld, 0, w_s, p->h_s, 1,
+                 static_cast<char*>(grad_input) + (size_t)r0 * p->h_s * s, p->h_s, rows, p->h_s,
+                 p->v, 0, 1, status, stream);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
-    // grad_weight (+)= dZ^T . X_s; the first chunk overwrites
-    GemmArgs gw{};
-    gw.a = zs; gw.sam = 1; gw.sak = L.ld;
-    gw.b = xs_c; gw.sbn = 1; gw.sbk = p->h_s;
-    gw.c = grad_weight; gw.ldc = p->h_s;
-    gw.m = p->v; gw.n = p->h_s; gw.k = rows; gw.accumulate = chunk > 0 ? 1 : 0;
-    trace_begin(FLJSD_KERNEL_GEMM_GRAD_WEIGHT, stream);
-    e = launch_gemm_simt(p->dtype, gw, stream);
-    trace_end(FLJSD_KERNEL_GEMM_GRAD_WEIGHT, stream);
+    // grad_weight (+)= dZ^T . X_s: both operands stored with the chunk rows as
+    // the outer dimension (M-major A, N-major B); the first chunk overwrites
+    e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_WEIGHT, zs, L.ld, 1, xs_c, p->h_s, 1,
+                 grad_weight, p->h_s, p->v, p->h_s, rows, chunk > 0 ? 1 : 0, 1, status, stream);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
   }
 
@@ -281,6 +290,37 @@ fljsd_status fljsd_backward(const fljsd_problem* p, const float* grad_output, vo
   if (launch_scale(p->dtype, grad_weight, p->v * p->h_s, grad_output, stream) != cudaSuccess)
     return FLJSD_ERR_CUDA;
   return FLJSD_OK;
+}
+
+fljsd_status fljsd_workspace_status(const fljsd_plan_t* plan, const void* workspace,
+                                    fljsd_stream_t stream_, int32_t* device_status) {
+  if (!plan || !workspace || !device_status || plan->status_offset + 4 > plan->workspace_bytes)
+    return FLJSD_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, static_cast<const char*>(workspace) + plan->status_offset, sizeof(v),
+                      cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return FLJSD_ERR_CUDA;
+  *device_status = v;
+  return FLJSD_OK;
+}
+
+fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const void* b,
+                             int64_t ldb, int32_t b_mn, void* d, int64_t ldd, int64_t m,
+                             int64_t n, int64_t k, int32_t accumulate, int32_t* status,
+                             fljsd_stream_t stream_) {
+  if (!a || !b || !d || m <= 0 || n <= 0 || k <= 0) return FLJSD_ERR_INVALID_ARG;
+  if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1) || (accumulate != 0 && accumulate != 1))
+    return FLJSD_ERR_INVALID_ARG;
+  if (lda < (a_mn ? m : k) || ldb < (b_mn ? n : k) || ldd < n) return FLJSD_ERR_INVALID_ARG;
+  TcGemmArgs t{a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, 1, status};
+  if (!tc_gemm_supported(t)) return FLJSD_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  trace_begin(FLJSD_KERNEL_SMALL, stream);
+  cudaError_t e = launch_gemm_tc(t, stream);
+  trace_end(FLJSD_KERNEL_SMALL, stream);
+  return e == cudaSuccess ? FLJSD_OK : FLJSD_ERR_CUDA;
 }
 
 int64_t fljsd_launch_count(void) { return g_launches.load(); }

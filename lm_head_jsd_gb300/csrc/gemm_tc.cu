@@ -1,0 +1,494 @@
+// bf16 GEMM on the 5th-generation tensor cores (sm_103a): D (+)= A . B^T.
+//
+// Persistent, warp-specialised kernel, one CTA per SM:
+//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a 4-stage
+//               shared-memory ring (mbarrier complete_tx).
+//   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), tile
+//               128 x 256 x 16, accumulating in tensor memory; two 256-column
+//               accumulators so the epilogue of tile i overlaps the main loop
+//               of tile i+1. Warp 1 also allocates / frees the 512 TMEM columns.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, rounding to bf16 (or
+//               fp32 read-modify-write of the stored bf16 value for
+//               accumulation), 16-byte stores.
+// Operands may be K-major (the contraction dimension contiguous) or MN-major;
+// the three contractions of the fused-linear JSD need: logits = X . W^T
+// (both K-major), grad_input = dZ . W (B MN-major), grad_weight = dZ^T . X
+// (both MN-major).
+//
+// Every wait on an mbarrier is bounded in time; on expiry the kernel records
+// FLJSD_ERR_TIMEOUT in a device status word, stops issuing work, drains what
+// it issued (again bounded) and frees its tensor memory.
+#include "internal.cuh"
+#include "gemm_tc.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace fljsd {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int ACC_COLS = BN;                    // fp32 accumulator columns per tile
+constexpr int TMEM_COLS = 2 * ACC_COLS;         // double-buffered accumulator
+constexpr int THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr unsigned long long kTimeoutNs = 10ull * 1000 * 1000 * 1000;  // 10 s
+
+// ---- PTX wrappers -----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Shared-memory control block.
+struct Ctrl {
+  unsigned long long full[STAGES];
+  unsigned long long empty[STAGES];
+  unsigned long long tmem_full[2];
+  unsigned long long tmem_empty[2];
+  unsigned long long drain;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+static_assert(sizeof(Ctrl) <= 256, "control block");
+
+// Bounded wait: true when the phase completed, false on timeout or abort
+// (then the abort flag is set and the status word records the timeout).
+__device__ __forceinline__ bool wait_bar(Ctrl* cb, uint32_t bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (cb->abort) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        cb->abort = 1;
+        if (status) atomicExch(status, (int)FLJSD_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor (sm_100 family):
+// [0,14) start >> 4, [16,30) leading-dimension byte offset >> 4,
+// [32,46) stride-dimension byte offset >> 4, [46,48) version = 1,
+// [49,52) base offset = 0, [52] LBO mode = 0, [61,64) layout: 2 = 128B swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32 ([4,6) = 1), A and B bf16
+// ([7,10) = 1, [10,13) = 1), A / B major ([15], [16]: 1 = MN-major),
+// N >> 3 at [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t instr_desc(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit accumulators: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+struct KParams {
+  int64_t m, n, k;
+  int64_t ldd;
+  int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
+  int raster_n_fastest;
+  int accumulate;
+  int* status;
+};
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              __nv_bfloat16* __restrict__ D, KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  Ctrl* cb = reinterpret_cast<Ctrl*>(gbase + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&cb->full[s]), 1);
+      mbar_init(smem_u32(&cb->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&cb->tmem_full[a]), 1);
+      mbar_init(smem_u32(&cb->tmem_empty[a]), 4);
+    }
+    mbar_init(smem_u32(&cb->drain), 1);
+    cb->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&cb->tmem_base)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = cb->tmem_base;
+
+  auto tile_coords = [&](int t, int& mb, int& nb) {
+    if (p.raster_n_fastest) {
+      nb = t % p.num_n_blocks;
+      mb = t / p.num_n_blocks;
+    } else {
+      mb = t % p.num_m_blocks;
+      nb = t / p.num_m_blocks;
+    }
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_parity[STAGES];
+      bool issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = false;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, mb, nb);
+        const int m0 = mb * BM, n0 = nb * BN;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!wait_bar(cb, smem_u32(&cb->empty[stage]), phase ^ 1u, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&cb->full[stage]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const int k0 = kb * BK;
+          if (A_MN) {
+            tma_load_2d(sa, &tmA, fb, m0, k0);
+            tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, k0);
+          } else {
+            tma_load_2d(sa, &tmA, fb, k0, m0);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tmB, fb, n0 + 64 * j, k0);
+          } else {
+            tma_load_2d(sb, &tmB, fb, k0, n0);
+          }
+          issued[stage] = true;
+          issued_parity[stage] = phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // drain: every issued copy has landed before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s]) wait_bar(cb, smem_u32(&cb->full[s]), issued_parity[s], p.status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = instr_desc(A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      bool any = false;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!wait_bar(cb, smem_u32(&cb->tmem_empty[acc]), acc_phase ^ 1u, p.status)) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + acc * ACC_COLS;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!wait_bar(cb, smem_u32(&cb->full[stage]), phase, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            uint64_t ad, bd;
+            if (A_MN)  // 16 k-rows of 128 B per step; MN atoms 8 KB apart
+              ad = smem_desc(sa + kk * (UMMA_K * 128), 8192, 1024);
+            else  // 32 bytes of k per step inside the 128-byte swizzled row
+              ad = smem_desc(sa + kk * (UMMA_K * 2), 16, 1024);
+            if (B_MN)
+              bd = smem_desc(sb + kk * (UMMA_K * 128), 8192, 1024);
+            else
+              bd = smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
+            mma_bf16(tmem_d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&cb->empty[stage]));  // frees the stage once read
+          any = true;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&cb->tmem_full[acc]));
+      }
+      if (any) {
+        // all issued MMAs have completed before tensor memory is released
+        mma_commit(smem_u32(&cb->drain));
+        wait_bar(cb, smem_u32(&cb->drain), 0, p.status);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int sub = warp & 3;  // TMEM lane quarter this warp may access
+    int local = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+      int mb, nb;
+      tile_coords(t, mb, nb);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      bool ok = true;
+      if (lane == 0) ok = wait_bar(cb, smem_u32(&cb->tmem_full[acc]), acc_phase, p.status);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const int64_t row = (int64_t)mb * BM + sub * 32 + lane;
+      const bool row_ok = row < p.m;
+      __nv_bfloat16* drow = D + row * p.ldd;
+      for (int c = 0; c < ACC_COLS / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem_base + ((uint32_t)(sub * 32) << 16) + acc * ACC_COLS + c * 32, v);
+        if (!row_ok) continue;
+        const int64_t col0 = (int64_t)nb * BN + c * 32;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t col = col0 + q * 8;
+          if (col >= p.n) break;
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = v[q * 8 + e];
+          __nv_bfloat16* dst = drow + col;
+          if (col + 8 <= p.n) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            if (p.accumulate) {
+              const uint4 o = *d4;
+              const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                x[2 * e] += bf16_lo(ow[e]);
+                x[2 * e + 1] += bf16_hi(ow[e]);
+              }
+            }
+            *d4 = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                             pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+          } else {
+            for (int e = 0; e < 8 && col + e < p.n; ++e) {
+              float y = x[e];
+              if (p.accumulate) y += __bfloat162float(dst[e]);
+              dst[e] = __float2bfloat16_rn(y);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&cb->tmem_empty[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS));
+  }
+}
+
+// ---- host: tensor maps ------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer x inner] matrix with row stride
+// ld elements; box = box_inner x box_outer; 128-byte swizzle; zero fill.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
+              int box_inner, int box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool A_MN, bool B_MN>
+cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, __nv_bfloat16* d,
+                     const KParams& p, cudaStream_t st) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<A_MN, B_MN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  k_gemm_tc<A_MN, B_MN><<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, d, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_gemm_supported(const TcGemmArgs& g) {
+  auto al = [](const void* q) { return ((uintptr_t)q & 15u) == 0; };
+  return g.m > 0 && g.n > 0 && g.k > 0 && al(g.a) && al(g.b) && al(g.d) && g.lda % 8 == 0 &&
+         g.ldb % 8 == 0 && g.ldd % 8 == 0 && g.m < (1ll << 31) && g.n < (1ll << 31) &&
+         g.k < (1ll << 31);
+}
+
+cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
+  if (!tc_gemm_supported(g)) return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  bool ok;
+  if (g.a_mn)  // A stored [k x m]
+    ok = make_map(&ma, g.a, g.m, g.k, g.lda, 64, 64);
+  else  // A stored [m x k]
+    ok = make_map(&ma, g.a, g.k, g.m, g.lda, BK, BM);
+  if (!ok) return cudaErrorInvalidValue;
+  if (g.b_mn)  // B stored [k x n]
+    ok = make_map(&mb, g.b, g.n, g.k, g.ldb, 64, 64);
+  else  // B stored [n x k]
+    ok = make_map(&mb, g.b, g.k, g.n, g.ldb, BK, BN);
+  if (!ok) return cudaErrorInvalidValue;
+  KParams p{};
+  p.m = g.m;
+  p.n = g.n;
+  p.k = g.k;
+  p.ldd = g.ldd;
+  p.num_m_blocks = (int)((g.m + BM - 1) / BM);
+  p.num_n_blocks = (int)((g.n + BN - 1) / BN);
+  p.num_k_blocks = (int)((g.k + BK - 1) / BK);
+  const int64_t tiles = (int64_t)p.num_m_blocks * p.num_n_blocks;
+  if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
+  p.num_tiles = (int)tiles;
+  p.raster_n_fastest = g.raster_n_fastest;
+  p.accumulate = g.accumulate;
+  p.status = g.status;
+  auto* d = reinterpret_cast<__nv_bfloat16*>(g.d);
+  if (!g.a_mn && !g.b_mn) return launch_t<false, false>(ma, mb, d, p, st);
+  if (!g.a_mn && g.b_mn) return launch_t<false, true>(ma, mb, d, p, st);
+  if (g.a_mn && g.b_mn) return launch_t<true, true>(ma, mb, d, p, st);
+  return launch_t<true, false>(ma, mb, d, p, st);
+}
+
+}  // namespace fljsd

@@ -1,0 +1,29 @@
+// Tensor-core GEMM interface (internal). See gemm_tc.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fljsd {
+
+// D[m x n] (+)= A . B^T, bf16 operands and output, fp32 accumulation.
+//   a_mn == 0: A is stored [m x k] row-major (k contiguous), row stride lda
+//   a_mn == 1: A is stored [k x m] row-major (m contiguous), row stride lda
+//   b_mn == 0: B is stored [n x k] row-major, row stride ldb
+//   b_mn == 1: B is stored [k x n] row-major, row stride ldb
+//   D is stored [m x ldd] row-major.
+// Requirements: 16-byte aligned pointers, lda / ldb / ldd multiples of 8.
+struct TcGemmArgs {
+  const void* a; int64_t lda; int a_mn;
+  const void* b; int64_t ldb; int b_mn;
+  void* d; int64_t ldd;
+  int64_t m, n, k;
+  int accumulate;        // 1: D = D + A.B^T (fp32 add, one rounding)
+  int raster_n_fastest;  // tile order: 1 walks n-blocks fastest, 0 m-blocks fastest
+  int* status;           // device word that receives FLJSD_ERR_TIMEOUT, or null
+};
+
+bool tc_gemm_supported(const TcGemmArgs& g);
+cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st);
+
+}  // namespace fljsd

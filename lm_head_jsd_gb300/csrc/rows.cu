@@ -132,49 +132,62 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
 }
 
 // ---- per-element branch arithmetic (log2 units) -----------------------------
-// X2 = log2 Q (student), Y2 = log2 P (teacher).
-// BRANCH 0: forward KL(P||Q); 1: reverse KL(Q||P); 2: generalized JSD.
-// Returns the per-element loss (log2 units, i.e. loss / ln 2) and, for the
-// generalized branch, the per-element log-prob gradient dX (also / ln 2).
-template <int BRANCH>
-__device__ __forceinline__ void elem_loss(float X2, float Y2, float beta, float omb,
+// Y2 = log2 P (teacher) and d = X2 - Y2 = log2(Q / P), where X2 = log2 Q is the
+// student log-prob. Working from d keeps the generalized branch accurate when
+// P and Q are close: with u = 2^d = Q / P and s = beta + (1 - beta) u = M / P,
+//   X2 - log2 M = d - log2 s,   Y2 - log2 M = -log2 s,
+// so no error of the absolute P or Q enters the log term, and Q = P u makes
+// the pair consistent. BRANCH 0: forward KL(P||Q); 1: reverse KL(Q||P);
+// 2: generalized JSD. PREC selects the accurate library exp2f/log2f (fp32
+// inputs) instead of the ex2/lg2 units (bf16 inputs).
+template <bool PREC>
+__device__ __forceinline__ float pexp2(float x) {
+  if (PREC) return exp2f(x);
+  return ex2(x);
+}
+template <bool PREC>
+__device__ __forceinline__ float plog2(float x) {
+  if (PREC) return log2f(x);
+  return lg2(x);
+}
+
+// Per-element loss (log2 units, loss / ln 2) and, for the generalized branch,
+// the log-prob gradient dX (also / ln 2). A tie (d == 0) contributes exactly 0.
+template <int BRANCH, bool PREC>
+__device__ __forceinline__ void elem_loss(float Y2, float d, float beta, float omb,
                                           float& ell, float& g) {
-  const float Q = ex2(X2), P = ex2(Y2);
+  ell = 0.f;
+  g = 0.f;
+  if (d == 0.f) return;
   if (BRANCH == 0) {
-    ell = (X2 == Y2) ? 0.f : P * (Y2 - X2);
-    g = 0.f;
+    ell = -pexp2<PREC>(Y2) * d;  // P (Y - X)
   } else if (BRANCH == 1) {
-    ell = (X2 == Y2) ? 0.f : Q * (X2 - Y2);
-    g = 0.f;
+    ell = pexp2<PREC>(Y2 + d) * d;  // Q (X - Y)
   } else {
-    const float M = beta * P + omb * Q;
-    if (X2 == Y2 || M == 0.f) {
-      ell = 0.f;
-      g = 0.f;
-    } else {
-      const float lM = lg2(M);
-      g = omb * Q * (X2 - lM);
-      ell = beta * P * (Y2 - lM) + g;
-    }
+    const float P = pexp2<PREC>(Y2);
+    const float u = pexp2<PREC>(d);
+    const float ls = plog2<PREC>(fmaf(omb, u, beta));
+    g = omb * (P * u) * (d - ls);
+    ell = g - beta * P * ls;
   }
 }
 
-// dlogit of one element, before the row scale w_r / T (natural-log units).
-// L and S are the row loss and dX_sum in log2 units (/ ln 2).
-template <int BRANCH>
-__device__ __forceinline__ float elem_grad(float X2, float Y2, float beta, float omb,
-                                           float L2, float S2) {
+// dlogit of one element before the row scale w_r / T (natural-log units).
+// L2 and S2 are the row loss and dX_sum in log2 units.
+template <int BRANCH, bool PREC>
+__device__ __forceinline__ float elem_grad(float Y2, float d, float beta, float omb, float L2,
+                                           float S2) {
   const float ln2 = 0.6931471805599453f;
-  const float Q = ex2(X2);
   if (BRANCH == 0) {
-    return Q - ex2(Y2);
+    if (d == 0.f) return 0.f;
+    return pexp2<PREC>(Y2) * (pexp2<PREC>(d) - 1.f);  // Q - P
   } else if (BRANCH == 1) {
-    return Q * (ln2 * ((X2 - Y2) - L2));
+    return pexp2<PREC>(Y2 + d) * (ln2 * (d - L2));  // Q (X - Y - L)
   } else {
-    const float P = ex2(Y2);
-    const float M = beta * P + omb * Q;
-    float g = 0.f;
-    if (!(X2 == Y2 || M == 0.f)) g = omb * Q * (X2 - lg2(M));
+    const float P = pexp2<PREC>(Y2);
+    const float u = pexp2<PREC>(d);
+    const float Q = P * u;
+    const float g = (d == 0.f) ? 0.f : omb * Q * (d - plog2<PREC>(fmaf(omb, u, beta)));
     return ln2 * (g - Q * S2);
   }
 }
@@ -182,6 +195,7 @@ __device__ __forceinline__ float elem_grad(float X2, float Y2, float beta, float
 template <typename T, int BRANCH>
 __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
   using V = Vec<T>;
+  constexpr bool PREC = sizeof(T) == 4;
   constexpr int N = V::N;
   __shared__ MD sh_md[kWarps];
   __shared__ float2 sh_s[kWarps];
@@ -240,8 +254,9 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
     }
     const MD ra = block_md(ma, sh_md);
     const MD rb = block_md(mb, sh_md);
-    const float lse_a = ra.m + lg2(ra.d);  // log2-sum-exp2 of the scaled student logits
-    const float lse_b = rb.m + lg2(rb.d);
+    const float lse_a = ra.m + plog2<PREC>(ra.d);  // log2-sum-exp2 of the scaled student logits
+    const float lse_b = rb.m + plog2<PREC>(rb.d);
+    const float dlse = __fsub_rn(lse_a, lse_b);
 
     // ---- pass 2: loss and dX_sum ----
     float2 acc = make_float2(0.f, 0.f);
@@ -251,19 +266,21 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       V::load(zt + i * N, xt);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const float X2 = __fsub_rn(__fmul_rn(xs[k], c), lse_a);
-        const float Y2 = __fsub_rn(__fmul_rn(xt[k], c), lse_b);
+        const float as = __fmul_rn(xs[k], c), bs = __fmul_rn(xt[k], c);
+        const float Y2 = __fsub_rn(bs, lse_b);
+        const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
         float ell, g;
-        elem_loss<BRANCH>(X2, Y2, beta, omb, ell, g);
+        elem_loss<BRANCH, PREC>(Y2, d, beta, omb, ell, g);
         acc.x += ell;
         acc.y += g;
       }
     }
     for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-      const float X2 = __fsub_rn(__fmul_rn(V::one(zs + j), c), lse_a);
-      const float Y2 = __fsub_rn(__fmul_rn(V::one(zt + j), c), lse_b);
+      const float as = __fmul_rn(V::one(zs + j), c), bs = __fmul_rn(V::one(zt + j), c);
+      const float Y2 = __fsub_rn(bs, lse_b);
+      const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
       float ell, g;
-      elem_loss<BRANCH>(X2, Y2, beta, omb, ell, g);
+      elem_loss<BRANCH, PREC>(Y2, d, beta, omb, ell, g);
       acc.x += ell;
       acc.y += g;
     }
@@ -279,16 +296,18 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       V::load(zt + i * N, xt);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const float X2 = __fsub_rn(__fmul_rn(xs[k], c), lse_a);
-        const float Y2 = __fsub_rn(__fmul_rn(xt[k], c), lse_b);
-        xs[k] = elem_grad<BRANCH>(X2, Y2, beta, omb, L2, S2) * scale;
+        const float as = __fmul_rn(xs[k], c), bs = __fmul_rn(xt[k], c);
+        const float Y2 = __fsub_rn(bs, lse_b);
+        const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
+        xs[k] = elem_grad<BRANCH, PREC>(Y2, d, beta, omb, L2, S2) * scale;
       }
       V::store(zs + i * N, xs);
     }
     for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-      const float X2 = __fsub_rn(__fmul_rn(V::one(zs + j), c), lse_a);
-      const float Y2 = __fsub_rn(__fmul_rn(V::one(zt + j), c), lse_b);
-      V::put(zs + j, elem_grad<BRANCH>(X2, Y2, beta, omb, L2, S2) * scale);
+      const float as = __fmul_rn(V::one(zs + j), c), bs = __fmul_rn(V::one(zt + j), c);
+      const float Y2 = __fsub_rn(bs, lse_b);
+      const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
+      V::put(zs + j, elem_grad<BRANCH, PREC>(Y2, d, beta, omb, L2, S2) * scale);
     }
     __syncthreads();
   }
@@ -307,7 +326,8 @@ __global__ void k_count_valid(const int64_t* labels, int64_t bt, int64_t ignore_
   if (threadIdx.x == 0) {
     int t = 0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += sh[w];
-    *n_valid = t;
+    n_valid[0] = t;
+    n_valid[1] = FLJSD_OK;  // the device status word that follows the count
   }
 }
 

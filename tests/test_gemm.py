@@ -1,0 +1,77 @@
+"""The tensor-core GEMM building block (fljsd_gemm_bf16) against a plain PyTorch
+fp32 reference of the same contraction, for every operand layout the path uses,
+ragged shapes, multi-tile shapes and the accumulate (beta = 1) epilogue."""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # (m, n, k)
+    (1, 8, 8), (7, 9, 24), (128, 256, 64), (300, 1000, 200), (129, 257, 65),
+    (1024, 2048, 1024), (64, 4096, 2048), (2000, 512, 4096),
+]
+
+
+def _operand(mn_major, outer, inner, gen):
+    """bf16 matrix stored [outer x inner] row-major, with values in N(0, 1)."""
+    return torch.randn(outer, inner, generator=gen, device="cuda").to(torch.bfloat16)
+
+
+def _ref(a, a_mn, b, b_mn):
+    A = a.float().t() if a_mn else a.float()  # [m x k]
+    B = b.float().t() if b_mn else b.float()  # [n x k]
+    return A @ B.t()
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_gemm_layouts(a_mn, b_mn, shape):
+    from lm_head_jsd_gb300 import fljsd_gemm_bf16
+
+    m, n, k = shape
+    g = torch.Generator(device="cuda").manual_seed(m * 7 + n * 3 + k)
+    a = _operand(a_mn, k if a_mn else m, m if a_mn else k, g)
+    b = _operand(b_mn, k if b_mn else n, n if b_mn else k, g)
+    d = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fljsd_gemm_bf16(a, a.shape[1], a_mn, b, b.shape[1], b_mn, d, n, m, n, k, 0, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    ref = _ref(a, a_mn, b, b_mn)
+    err = (d.float() - ref).norm() / ref.norm()
+    assert err < 4e-3, float(err)
+    # accumulate: D = D + A.B^T
+    d0 = d.clone()
+    fljsd_gemm_bf16(a, a.shape[1], a_mn, b, b.shape[1], b_mn, d, n, m, n, k, 1, status)
+    torch.cuda.synchronize()
+    ref2 = d0.float() + ref
+    err = (d.float() - ref2).norm() / ref2.norm()
+    assert err < 4e-3, float(err)
+
+
+def test_gemm_strided_output_and_guard():
+    """Output with a row stride larger than n: the padding columns and the rows
+    past m are never written."""
+    from lm_head_jsd_gb300 import fljsd_gemm_bf16
+
+    m, n, k, ldd = 200, 1000, 320, 1032
+    g = torch.Generator(device="cuda").manual_seed(5)
+    a = torch.randn(m, k, generator=g, device="cuda").to(torch.bfloat16)
+    b = torch.randn(n, k, generator=g, device="cuda").to(torch.bfloat16)
+    buf = torch.full((m + 3, ldd), 7.0, dtype=torch.bfloat16, device="cuda")
+    fljsd_gemm_bf16(a, k, 0, b, k, 0, buf, ldd, m, n, k, 0)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:, n:] == 7.0) and torch.all(buf[m:] == 7.0)
+    ref = a.float() @ b.float().t()
+    err = (buf[:m, :n].float() - ref).norm() / ref.norm()
+    assert err < 4e-3
+
+
+def test_gemm_rejects_bad_arguments():
+    from lm_head_jsd_gb300 import fljsd_gemm_bf16
+
+    a = torch.zeros(16, 16, dtype=torch.bfloat16, device="cuda")
+    assert fljsd_gemm_bf16(a, 16, 0, a, 16, 0, a, 16, 16, 16, 0, check=False) == 1  # k = 0
+    assert fljsd_gemm_bf16(a, 12, 0, a, 16, 0, a, 16, 16, 16, 12, check=False) == 1  # lda % 8
+    assert fljsd_gemm_bf16(a, 16, 2, a, 16, 0, a, 16, 16, 16, 16, check=False) == 1
