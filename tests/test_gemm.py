@@ -14,8 +14,13 @@ SHAPES = [
 
 
 def _operand(mn_major, outer, inner, gen):
-    """bf16 matrix stored [outer x inner] row-major, with values in N(0, 1)."""
-    return torch.randn(outer, inner, generator=gen, device="cuda").to(torch.bfloat16)
+    """bf16 matrix stored [outer x inner] row-major with values in N(0, 1), as a
+    view of storage whose row stride is a multiple of 8 elements; the padding
+    holds NaN so that reading it would show."""
+    ld = -(-inner // 8) * 8
+    buf = torch.full((outer, ld), float("nan"), dtype=torch.bfloat16, device="cuda")
+    buf[:, :inner] = torch.randn(outer, inner, generator=gen, device="cuda").to(torch.bfloat16)
+    return buf[:, :inner], ld
 
 
 def _ref(a, a_mn, b, b_mn):
@@ -31,11 +36,13 @@ def test_gemm_layouts(a_mn, b_mn, shape):
 
     m, n, k = shape
     g = torch.Generator(device="cuda").manual_seed(m * 7 + n * 3 + k)
-    a = _operand(a_mn, k if a_mn else m, m if a_mn else k, g)
-    b = _operand(b_mn, k if b_mn else n, n if b_mn else k, g)
-    d = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    a, lda = _operand(a_mn, k if a_mn else m, m if a_mn else k, g)
+    b, ldb = _operand(b_mn, k if b_mn else n, n if b_mn else k, g)
+    ldd = -(-n // 8) * 8
+    dbuf = torch.empty(m, ldd, dtype=torch.bfloat16, device="cuda")
+    d = dbuf[:, :n]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fljsd_gemm_bf16(a, a.shape[1], a_mn, b, b.shape[1], b_mn, d, n, m, n, k, 0, status)
+    fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, 0, status)
     torch.cuda.synchronize()
     assert status.item() == 0
     ref = _ref(a, a_mn, b, b_mn)
@@ -43,7 +50,7 @@ def test_gemm_layouts(a_mn, b_mn, shape):
     assert err < 4e-3, float(err)
     # accumulate: D = D + A.B^T
     d0 = d.clone()
-    fljsd_gemm_bf16(a, a.shape[1], a_mn, b, b.shape[1], b_mn, d, n, m, n, k, 1, status)
+    fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, 1, status)
     torch.cuda.synchronize()
     ref2 = d0.float() + ref
     err = (d.float() - ref2).norm() / ref2.norm()
