@@ -1,0 +1,414 @@
+"""Benchmark of the fused-linear JSD forward + backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload headline]
+    python bench.py --impl reference ...   # the float64 CPU oracle on host cores
+
+One step is fljsd_forward + fljsd_backward (upstream gradient 1) over one batch
+of synthetic inputs resident in HBM: both logits GEMMs, the three passes over
+the vocabulary, grad_input and grad_weight, the loss reduction and the
+backward scaling. Prints one JSON line (rank 0). Under torchrun each rank runs
+an independent replica on its own GPU (the loss shards by rows, but this build
+runs replicas only: no collective), and the value is the tokens all ranks
+processed divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused-linear-JSD fwd+bwd tokens/s at H=4096,V=128256 bf16; % bf16 TC roofline"
+# The pages' own number for this workload (H100 80GB HBM3, BT=8192, one chunk,
+# 60.62 ms per full pass): context on another machine, not the target.
+PAGES_MS_ONE_CHUNK = 60.62
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _gpu_index(torch, dev) -> str:
+    """nvidia-smi identifier of the device: its PCI address when torch exposes
+    it, else its index among the visible devices."""
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        return f"{int(pr.pci_domain_id):08X}:{int(pr.pci_bus_id):02X}:{int(pr.pci_device_id):02X}.0"
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[dev.index or 0]
+    return str(dev.index or 0)
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of the same workload
+# ---------------------------------------------------------------------------
+def cpu_baseline(w, x_s, w_s, x_t, w_t, labels, budget_s: float, block: int = 16):
+    """Times the float64 oracle, as it stands, on blocks of rows of the workload
+    until about `budget_s` seconds of CPU work; returns tokens (rows) / s."""
+    import numpy as np
+
+    import oracle
+
+    f64 = lambda t: t.detach().cpu().double().numpy()  # noqa: E731
+    ws64, wt64 = f64(w_s), f64(w_t)
+    lab = None if labels is None else labels.cpu().numpy()
+    rows_done, elapsed = 0, 0.0
+    r0 = 0
+    while elapsed < budget_s and r0 < w.bt:
+        r1 = min(w.bt, r0 + block)
+        xs, xt = f64(x_s[r0:r1]), f64(x_t[r0:r1])
+        lb = None if lab is None else lab[r0:r1]
+        t0 = time.perf_counter()
+        oracle.fljsd_ref(xs, ws64, xt, wt64, lb, beta=w.beta, temperature=w.temperature,
+                         reduction=w.reduction)
+        elapsed += time.perf_counter() - t0
+        rows_done += r1 - r0
+        r0 = r1
+    del ws64, wt64
+    cores = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+
+        cores = max((i.get("num_threads", 0) for i in threadpool_info()), default=cores) or cores
+    except Exception:
+        pass
+    return {"value": rows_done / elapsed, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows_done} of {w.bt} rows of the {w.name} workload in blocks of {block} "
+                      f"(full V={w.v}, H_s={w.h_s}, H_t={w.h_t}), float64 NumPy, "
+                      f"{elapsed:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="headline")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--chunk-rows", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline field (0 disables)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--ref-rows", type=int, default=16,
+                    help="rows per step of the reference (oracle) arm")
+    args = ap.parse_args()
+
+    import torch
+
+    import jsd_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = jsd_inputs.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, w, world)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    import lm_head_jsd_gb300 as fl
+    from lm_head_jsd_gb300 import FusedLinearJSD
+
+    x_s, w_s, x_t, w_t, labels = jsd_inputs.make_inputs(w, str(dev))
+    run = FusedLinearJSD(w.bt, w.h_s, w.h_t, w.v, w.torch_dtype, beta=w.beta,
+                         temperature=w.temperature, reduction=w.reduction,
+                         chunk_rows=args.chunk_rows, device=dev)
+    loss, gi, gw = run.alloc_outputs()
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        run.forward(x_s, w_s, x_t, w_t, labels, out=(loss, gi, gw), stream=stream)
+        run.backward(one, gi, gw, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region ----
+    clocks = ClockSampler(_gpu_index(torch, dev))
+    fl.fljsd_trace_enable(args.steps * (5 * run.plan.num_chunks + 4) + 16)
+    fl.fljsd_trace_reset()
+    n_launch0 = fl.fljsd_launch_count()
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    launches = fl.fljsd_launch_count() - n_launch0
+    ms_total = ev0.elapsed_time(ev1)
+    kinds = {}
+    for k in ("gemm_logits", "jsd_rows", "gemm_grad_input", "gemm_grad_weight", "small"):
+        kinds[k] = fl.fljsd_trace_read(k)
+    fl.fljsd_trace_enable(0)
+    status = fl.fljsd_workspace_status(run.plan, run.workspace, stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    if dist:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * w.bt / (ms_step / 1e3)
+
+    # ---- roofline of the dominant kernel (the tensor-core GEMM) ----
+    peaks = _peaks()
+    gemm_ms = sum(kinds[k][0] for k in ("gemm_logits", "gemm_grad_input", "gemm_grad_weight"))
+    gemm_n = sum(kinds[k][1] for k in ("gemm_logits", "gemm_grad_input", "gemm_grad_weight"))
+    flop_step = w.flops()
+    steps_traced = gemm_n / (4 * run.plan.num_chunks) if gemm_n else 0
+    gemm_flop_per_launch = flop_step / (4 * run.plan.num_chunks)
+    gemm_avg_ms = gemm_ms / gemm_n if gemm_n else float("nan")
+    achieved = gemm_flop_per_launch / (gemm_avg_ms / 1e3) / 1e12
+    peak_tc = peaks["bf16_tflops_sustained"]
+    s = 2 if w.dtype == "bf16" else 4
+    jsd_ms, jsd_n = kinds["jsd_rows"]
+    jsd_bytes = 3 * w.bt * w.v * s / run.plan.num_chunks  # read Z_s, Z_t once; write dZ once
+    jsd_gbs = jsd_bytes / (jsd_ms / jsd_n / 1e3) / 1e9 if jsd_n else float("nan")
+    step_roof_ms = max(flop_step / (peak_tc * 1e12), 11 * w.bt * w.v * s / (peaks["hbm_gbs"] * 1e9)) * 1e3
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": round(value / (w.bt / (PAGES_MS_ONE_CHUNK / 1e3)), 3)
+        if w.name == "headline" else None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}: BT={w.bt} H_s={w.h_s} H_t={w.h_t} V={w.v} {w.dtype} "
+                               f"beta={w.beta} T={w.temperature} {w.reduction}",
+                   "global_batch": w.bt * world, "seq_len": None,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "chunk_rows": int(run.plan.chunk_rows), "num_chunks": int(run.plan.num_chunks),
+                   "l2": "inputs larger than L2 (W_s, W_t 1 GB each; logits buffers "
+                         f"{run.plan.logits_bytes / 1e9:.1f} GB)"},
+        "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (4 launches per chunk)",
+                     "achieved": round(achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tc, 4), "traffic": None,
+                     "peak_kind": f"bf16 sustained ({peaks['source']})"},
+        "roofline_step": {"flop": flop_step, "roofline_ms": round(step_roof_ms, 3),
+                          "frac": round(step_roof_ms / ms_step, 4),
+                          "peak": f"bf16 sustained {peak_tc} TFLOP/s ({peaks['source']})"},
+        "roofline_jsd": {"bound": "hbm", "achieved": round(jsd_gbs, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(jsd_gbs / peaks["hbm_gbs"], 4),
+                         "algorithmic_bytes": "3*C*V*s per launch"},
+        "kernel_ms_per_step": {k: round(v[0] / max(steps_traced, 1), 4) for k, v in kinds.items()},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if args.e2e_steps > 0:
+        out["e2e"] = run_e2e(torch, run, w, x_s, w_s, x_t, w_t, labels, args.e2e_steps, dist,
+                             world, dev)
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        out["cpu_baseline"] = cpu_baseline(w, x_s, w_s, x_t, w_t, labels, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(torch, run, w, x_s, w_s, x_t, w_t, labels, steps, dist, world, dev):
+    """The same step through the public API with the per-step inputs (hidden
+    states and labels) in pinned host memory: H2D copies, forward, backward and
+    the D2H read of the loss are all inside the timed region. The lm_head
+    weights stay resident (they are parameters, not per-step inputs)."""
+    hx_s = x_s.cpu().pin_memory()
+    hx_t = x_t.cpu().pin_memory()
+    hlab = None if labels is None else labels.cpu().pin_memory()
+    host_loss = torch.empty(run.alloc_outputs()[0].shape, dtype=torch.float32).pin_memory()
+    dx_s = torch.empty_like(x_s)
+    dx_t = torch.empty_like(x_t)
+    dlab = None if labels is None else torch.empty_like(labels)
+    loss, gi, gw = run.alloc_outputs()
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dx_s.copy_(hx_s, non_blocking=True)
+        dx_t.copy_(hx_t, non_blocking=True)
+        if dlab is not None:
+            dlab.copy_(hlab, non_blocking=True)
+        run.forward(dx_s, w_s, dx_t, w_t, dlab, out=(loss, gi, gw), stream=stream)
+        run.backward(one, gi, gw, stream=stream)
+        host_loss.copy_(loss, non_blocking=True)
+        stream.synchronize()
+        return float(host_loss[0])
+
+    for _ in range(2):
+        step()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = hx_s.numel() * hx_s.element_size() + hx_t.numel() * hx_t.element_size() + (
+        0 if hlab is None else hlab.numel() * 8)
+    return {"value": round(world * w.bt / (ms / 1e3), 1), "unit": "tokens/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": host_loss.numel() * 4,
+            "what": "pinned-host X_s, X_t, labels -> device; fljsd_forward + fljsd_backward; "
+                    "loss -> host; wall clock per step, stream synchronised every step"}
+
+
+def run_reference(args, w, world):
+    """The reference arm: the float64 CPU oracle, as it stands, on the host cores,
+    each step a bounded sample of `--ref-rows` rows of the same workload."""
+    import numpy as np
+
+    import jsd_inputs
+    import oracle
+
+    import torch
+
+    # the same draw as the native arm (a CUDA generator when a GPU is present)
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x_s, w_s, x_t, w_t, labels = (None if t is None else t.cpu()
+                                  for t in jsd_inputs.make_inputs(w, gen_dev))
+    f64 = lambda t: t.detach().double().numpy()  # noqa: E731
+    ws64, wt64 = f64(w_s), f64(w_t)
+    lab = None if labels is None else labels.numpy()
+    rows = args.ref_rows
+
+    def step(i):
+        r0 = (i * rows) % max(1, x_s.shape[0] - rows + 1)
+        oracle.fljsd_ref(f64(x_s[r0:r0 + rows]), ws64, f64(x_t[r0:r0 + rows]), wt64,
+                         None if lab is None else lab[r0:r0 + rows], beta=w.beta,
+                         temperature=w.temperature, reduction=w.reduction)
+
+    for i in range(max(args.warmup, 1)):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    sec = time.perf_counter() - t0
+    ms = sec * 1e3 / args.steps
+    value = rows / (ms / 1e3)
+    cores = os.cpu_count()
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+           "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 1),
+           "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": f"{w.name}: BT={w.bt} H_s={w.h_s} H_t={w.h_t} V={w.v} {w.dtype} "
+                                  f"beta={w.beta} T={w.temperature} {w.reduction}",
+                      "rows_per_step": rows},
+           "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
+                            "kind": "oracle",
+                            "sample": f"{rows} rows per step of the {w.name} workload "
+                                      f"(full V and H), float64 NumPy"},
+           "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
