@@ -347,3 +347,16 @@ def test_from_logits_matches_full_reference():
         np.testing.assert_allclose(a[0], b[0], rtol=1e-13)
         np.testing.assert_allclose(a[1], b[1], rtol=1e-12)
         np.testing.assert_allclose(a[2], b[2], rtol=1e-11, atol=1e-16)
+
+
+def test_rows_reference_matches_full_reference_rows():
+    from oracle import fljsd_rows_ref
+
+    x_s, w_s, x_t, w_t = _problem(18, bt=7, h=6, v=30)
+    _, gi, _ = fljsd_ref(x_s, w_s, x_t, w_t, beta=0.2, temperature=1.7, reduction="sum")
+    rows, _, _ = fljsd_ref(x_s, w_s, x_t, w_t, beta=0.2, temperature=1.7, reduction="none")
+    idx = [1, 4, 6]
+    L, dz, gir = fljsd_rows_ref(x_s[idx], w_s, x_t[idx], w_t, beta=0.2, temperature=1.7,
+                                row_scale=np.ones(3))
+    np.testing.assert_allclose(L, rows[idx], rtol=1e-13)
+    np.testing.assert_allclose(gir, gi[idx], rtol=1e-12)
