@@ -143,6 +143,34 @@ fljsd_status fljsd_forward(const fljsd_problem* problem, const fljsd_plan_t* pla
                            void* workspace, size_t workspace_bytes, fljsd_stream_t stream);
 
 /*
+ * fljsd_forward_noalloc -- fljsd_forward for callers that cannot allocate
+ * device memory (e.g. a plugin inside a host framework that owns every
+ * device allocation and passes in only input and output buffers). The pages
+ * have no counterpart of this entry point; it is an addition of this library.
+ *
+ * Arguments are those of fljsd_forward without plan and workspace: the
+ * scratch lives in a fixed 64 MiB device array inside the library, which
+ * every GPU that loads the library holds until the process exits.
+ *   - The chunk rows are chosen to fit that array (problem->chunk_rows, if
+ *     > 0, must fit it). A problem whose scratch does not fit even one row
+ *     (2 * ceil8(v) * sizeof(dtype) bytes per row, plus 4 * bt bytes) returns
+ *     FLJSD_ERR_WORKSPACE before anything is launched.
+ *   - Every call shares the one array: calls whose work overlaps on the GPU
+ *     (different streams, different host threads) race; serialise them.
+ *     Nothing in the array has to start at zero: a call writes every byte it
+ *     reads, so what the previous call left there does not matter.
+ *   - The first call on a device (the current device) looks up the array's
+ *     device address with the CUDA runtime and caches it; make that first
+ *     call before any stream capture. It calls no cudaMalloc or cudaFree.
+ * Returns what fljsd_forward returns, and FLJSD_ERR_CUDA if the address
+ * lookup fails.
+ */
+fljsd_status fljsd_forward_noalloc(const fljsd_problem* problem, const void* x_s,
+                                   const void* w_s, const void* x_t, const void* w_t,
+                                   const int64_t* labels, const float* row_grad, float* loss,
+                                   void* grad_input, void* grad_weight, fljsd_stream_t stream);
+
+/*
  * fljsd_backward -- scale the gradients computed by fljsd_forward by the
  * upstream scalar gradient *grad_output (device fp32), in place, on `stream`.
  * The forward already holds the gradients for an upstream gradient of 1

@@ -8,6 +8,7 @@ from ._lib import (  # noqa: F401
     FljsdError,
     fljsd_backward,
     fljsd_forward,
+    fljsd_forward_noalloc,
     fljsd_gemm_bf16,
     fljsd_launch_count,
     fljsd_launch_count_reset,

@@ -55,6 +55,9 @@ def _load():
     lib.fljsd_forward.argtypes = [ctypes.POINTER(fljsd_problem), ctypes.POINTER(fljsd_plan_t),
                                   P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     lib.fljsd_forward.restype = ctypes.c_int
+    lib.fljsd_forward_noalloc.argtypes = [ctypes.POINTER(fljsd_problem), P, P, P, P, P, P, P, P,
+                                          P, P]
+    lib.fljsd_forward_noalloc.restype = ctypes.c_int
     lib.fljsd_backward.argtypes = [ctypes.POINTER(fljsd_problem), P, P, P, P]
     lib.fljsd_backward.restype = ctypes.c_int
     lib.fljsd_workspace_status.argtypes = [ctypes.POINTER(fljsd_plan_t), P, P,
@@ -131,6 +134,18 @@ def fljsd_forward(problem, plan, x_s, w_s, x_t, w_t, labels, row_grad, loss, gra
                            workspace_bytes, _stream(stream))
     if check and st != FLJSD_OK:
         raise FljsdError(st, "fljsd_forward")
+    return st
+
+
+def fljsd_forward_noalloc(problem, x_s, w_s, x_t, w_t, labels, row_grad, loss, grad_input,
+                          grad_weight, stream=None, check=True) -> int:
+    """fljsd_forward with the library's fixed device scratch instead of a
+    caller-provided workspace (for callers that cannot allocate)."""
+    st = lib.fljsd_forward_noalloc(ctypes.byref(problem), _ptr(x_s), _ptr(w_s), _ptr(x_t),
+                                   _ptr(w_t), _ptr(labels), _ptr(row_grad), _ptr(loss),
+                                   _ptr(grad_input), _ptr(grad_weight), _stream(stream))
+    if check and st != FLJSD_OK:
+        raise FljsdError(st, "fljsd_forward_noalloc")
     return st
 
 
