@@ -67,6 +67,8 @@ WORKLOADS = {
                               beta=0.1, temperature=2.0, ignore_frac=0.05),
     # the pages' benchmark shape: BT=8192, H=4096, V=128256, bf16
     "headline": Workload("headline", 6, 8192, 4096, 4096, 128256, "bf16"),
+    # the headline's H and V with BT=1024 (small enough for full profiler captures)
+    "headline_bt1024": Workload("headline_bt1024", 7, 1024, 4096, 4096, 128256, "bf16"),
 }
 
 
