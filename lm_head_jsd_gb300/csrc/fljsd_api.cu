@@ -81,8 +81,8 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 inline size_t dtype_size(int dt) { return dt == FLJSD_BF16 ? 2 : 4; }
 
 struct Layout {
-  int64_t ld;
-  size_t zs, zt, loss_rows, misc, total, logits_bytes, stats_bytes;
+  int64_t ld, ntiles;
+  size_t zs, zt, stats_s, stats_t, loss_rows, misc, total, logits_bytes, stats_bytes;
 };
 
 Layout layout_for(const fljsd_problem& p, int64_t chunk_rows) {
@@ -90,13 +90,18 @@ Layout layout_for(const fljsd_problem& p, int64_t chunk_rows) {
   L.ld = (p.v + 7) / 8 * 8;
   const size_t s = dtype_size(p.dtype);
   const size_t zbytes = align_up((size_t)chunk_rows * (size_t)L.ld * s);
+  // per-row, per-256-column-tile pass-1 partials written by the logits GEMMs
+  L.ntiles = (p.v + TC_TILE_N - 1) / TC_TILE_N;
+  const size_t sbytes = align_up((size_t)chunk_rows * (size_t)L.ntiles * sizeof(float2));
   L.zs = 0;
   L.zt = zbytes;
-  L.loss_rows = 2 * zbytes;
+  L.stats_s = 2 * zbytes;
+  L.stats_t = L.stats_s + sbytes;
+  L.loss_rows = L.stats_t + sbytes;
   L.misc = L.loss_rows + align_up((size_t)p.bt * sizeof(float));
   L.total = L.misc + kAlign;
   L.logits_bytes = 2 * (size_t)chunk_rows * (size_t)L.ld * s;
-  L.stats_bytes = align_up((size_t)p.bt * sizeof(float)) + kAlign;
+  L.stats_bytes = 2 * sbytes + align_up((size_t)p.bt * sizeof(float)) + kAlign;
   return L;
 }
 
@@ -122,15 +127,22 @@ inline bool aligned16(const void* q) { return ((uintptr_t)q & 15u) == 0; }
 // dimension as its outer (row) dimension. bf16 goes to the tensor cores
 // whenever the strides allow TMA (multiples of 8 elements); fp32 and the
 // remaining bf16 shapes use the CUDA-core kernel.
+// `stats` (optional) receives the per-row pass-1 partials of the output;
+// *stats_done tells whether they were produced (the tensor-core path only).
 cudaError_t run_gemm(int dtype, int kind, const void* a, int64_t lda, int a_mn, const void* b,
                      int64_t ldb, int b_mn, void* d, int64_t ldd, int64_t m, int64_t n, int64_t k,
-                     int accumulate, int raster_n_fastest, int* status, cudaStream_t st) {
+                     int accumulate, int raster_n_fastest, int* status, cudaStream_t st,
+                     float2* stats = nullptr, float stats_scale = 0.f,
+                     bool* stats_done = nullptr) {
+  if (stats_done) *stats_done = false;
   if (m <= 0 || n <= 0) return cudaSuccess;
   cudaError_t e;
   trace_begin(kind, st);
-  TcGemmArgs t{a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, raster_n_fastest, status};
+  TcGemmArgs t{a,        lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, raster_n_fastest,
+               status,   stats, stats_scale};
   if (dtype == FLJSD_BF16 && tc_gemm_supported(t)) {
     e = launch_gemm_tc(t, st);
+    if (stats_done) *stats_done = stats != nullptr;
   } else {
     GemmArgs g{};
     g.a = a; g.sam = a_mn ? 1 : lda; g.sak = a_mn ? lda : 1;
@@ -228,6 +240,8 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
   float* loss_rows = p->reduction == FLJSD_RED_NONE ? loss : reinterpret_cast<float*>(ws + L.loss_rows);
   int* n_valid = reinterpret_cast<int*>(ws + L.misc);
   int* status = n_valid + 1;  // device status word, reset by the row-count kernel
+  float2* stats_s = reinterpret_cast<float2*>(ws + L.stats_s);
+  float2* stats_t = reinterpret_cast<float2*>(ws + L.stats_t);
   const size_t s = dtype_size(p->dtype);
 
   cudaError_t e = launch_count_valid(labels, p->bt, p->ignore_index, n_valid, stream);
@@ -239,12 +253,15 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
     const char* xs_c = static_cast<const char*>(x_s) + (size_t)r0 * p->h_s * s;
     const char* xt_c = static_cast<const char*>(x_t) + (size_t)r0 * p->h_t * s;
 
-    // student and teacher logits, rounded to the input dtype (X . W^T, both K-major)
+    // student and teacher logits, rounded to the input dtype (X . W^T, both K-major),
+    // with the pass-1 partials of each row folded in the epilogue
+    const float c2 = (float)(1.4426950408889634 / (double)p->temperature);
+    bool st_s = false, st_t = false;
     e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_LOGITS, xs_c, p->h_s, 0, w_s, p->h_s, 0, zs, L.ld,
-                 rows, p->v, p->h_s, 0, 0, status, stream);
+                 rows, p->v, p->h_s, 0, 0, status, stream, stats_s, c2, &st_s);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
     e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_LOGITS, xt_c, p->h_t, 0, w_t, p->h_t, 0, zt, L.ld,
-                 rows, p->v, p->h_t, 0, 0, status, stream);
+                 rows, p->v, p->h_t, 0, 0, status, stream, stats_t, c2, &st_t);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
     // three passes over V; dlogits overwrite the student logits
@@ -253,7 +270,12 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
     ra.labels = labels; ra.ignore_index = p->ignore_index;
     ra.row_grad = p->reduction == FLJSD_RED_NONE ? row_grad : nullptr;
     ra.n_valid = n_valid; ra.loss_rows = loss_rows; ra.reduction = p->reduction;
-    ra.beta = p->beta; ra.inv_temperature = 1.0f / p->temperature;
+    ra.beta = p->beta; ra.inv_temperature = 1.0f / p->temperature; ra.scale_log2 = c2;
+    // the partials are used only when both GEMMs produced them (same code path
+    // for student and teacher, so equal logits give equal statistics)
+    ra.stats_s = (st_s && st_t) ? stats_s : nullptr;
+    ra.stats_t = (st_s && st_t) ? stats_t : nullptr;
+    ra.ntiles = L.ntiles;
     e = launch_jsd_rows(p->dtype, ra, stream);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
@@ -314,7 +336,7 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
   if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1) || (accumulate != 0 && accumulate != 1))
     return FLJSD_ERR_INVALID_ARG;
   if (lda < (a_mn ? m : k) || ldb < (b_mn ? n : k) || ldd < n) return FLJSD_ERR_INVALID_ARG;
-  TcGemmArgs t{a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, 1, status};
+  TcGemmArgs t{a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, 1, status, nullptr, 0.f};
   if (!tc_gemm_supported(t)) return FLJSD_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   trace_begin(FLJSD_KERNEL_SMALL, stream);

@@ -171,6 +171,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ float ex2f_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -181,6 +187,8 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 struct KParams {
   int64_t m, n, k;
   int64_t ldd;
+  float2* stats;       // [m x num_n_blocks] (max, sum 2^(x - max)) per row and tile, or null
+  float stats_scale;   // x = bf16(value) * stats_scale
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
   int raster_n_fastest;
   int accumulate;
@@ -348,11 +356,37 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t row = (int64_t)mb * BM + sub * 32 + lane;
       const bool row_ok = row < p.m;
       __nv_bfloat16* drow = D + row * p.ldd;
+      // running (max, sum 2^(x - max)) of this row over the tile's columns, on
+      // the values as stored (rounded to bf16) times stats_scale: pass 1 of the
+      // online softmax, done here while the tile is in registers
+      float st_m = -INFINITY, st_d = 0.f;
       for (int c = 0; c < ACC_COLS / 32; ++c) {
         float v[32];
         tmem_ld32(tmem_base + ((uint32_t)(sub * 32) << 16) + acc * ACC_COLS + c * 32, v);
         if (!row_ok) continue;
         const int64_t col0 = (int64_t)nb * BN + c * 32;
+        if (p.stats) {
+          float cm = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = (col0 + e < p.n)
+                ? __fmul_rn(__bfloat162float(__float2bfloat16_rn(v[e])), p.stats_scale)
+                : -INFINITY;
+            cm = fmaxf(cm, x);
+          }
+          if (cm > st_m) {
+            st_d = (st_m == -INFINITY) ? 0.f : st_d * ex2f_approx(st_m - cm);
+            st_m = cm;
+          }
+          float acc_d = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (col0 + e < p.n)
+              acc_d += ex2f_approx(
+                  __fmul_rn(__bfloat162float(__float2bfloat16_rn(v[e])), p.stats_scale) - st_m);
+          }
+          st_d += acc_d;
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int64_t col = col0 + q * 8;
@@ -383,6 +417,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
+      if (p.stats && row_ok) p.stats[row * p.num_n_blocks + nb] = make_float2(st_m, st_d);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&cb->tmem_empty[acc]));
@@ -484,6 +519,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.raster_n_fastest = g.raster_n_fastest;
   p.accumulate = g.accumulate;
   p.status = g.status;
+  p.stats = g.stats;
+  p.stats_scale = g.stats_scale;
   auto* d = reinterpret_cast<__nv_bfloat16*>(g.d);
   if (!g.a_mn && !g.b_mn) return launch_t<false, false>(ma, mb, d, p, st);
   if (!g.a_mn && g.b_mn) return launch_t<false, true>(ma, mb, d, p, st);

@@ -21,7 +21,14 @@ struct TcGemmArgs {
   int accumulate;        // 1: D = D + A.B^T (fp32 add, one rounding)
   int raster_n_fastest;  // tile order: 1 walks n-blocks fastest, 0 m-blocks fastest
   int* status;           // device word that receives FLJSD_ERR_TIMEOUT, or null
+  // Optional row statistics of the stored output (requires accumulate == 0):
+  // for row r and n-tile j (TC_TILE_N columns), stats[r * ceil(n / TC_TILE_N) + j]
+  // = (max_x, sum 2^(x - max_x)) over x = bf16(D[r, col]) * stats_scale.
+  float2* stats;
+  float stats_scale;
 };
+
+constexpr int TC_TILE_N = 256;
 
 bool tc_gemm_supported(const TcGemmArgs& g);
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st);

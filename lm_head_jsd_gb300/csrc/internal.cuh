@@ -34,9 +34,15 @@ struct JsdRowArgs {
   const float* row_grad; // [bt] or null (reduction NONE only)
   const int* n_valid;    // device scalar
   float* loss_rows;      // [bt], indexed by global row
+  // Pass-1 partials from the logits GEMM epilogue, or null (then pass 1 runs
+  // here): [rows x ntiles] (max, sum 2^(x - max)) of x = z * log2(e) / T.
+  const float2* stats_s;
+  const float2* stats_t;
+  int64_t ntiles;
   int reduction;
   float beta;
   float inv_temperature;
+  float scale_log2;  // log2(e) / T, the same constant the GEMM epilogue used
 };
 
 cudaError_t launch_count_valid(const int64_t* labels, int64_t bt, int64_t ignore_index,

@@ -16,7 +16,7 @@
 namespace fljsd {
 namespace {
 
-constexpr int kRowThreads = 512;
+constexpr int kRowThreads = 1024;
 constexpr int kWarps = kRowThreads / 32;
 
 // ---- hardware transcendental units (hand-written PTX) ----------------------
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
   __shared__ MD sh_md[kWarps];
   __shared__ float2 sh_s[kWarps];
 
-  const float c = a.inv_temperature * 1.4426950408889634f;  // log2(e) / T
+  const float c = a.scale_log2;  // log2(e) / T
   const float beta = a.beta, omb = 1.f - a.beta;
   const int64_t nvec = a.v / N;
   const int64_t tail0 = nvec * N;
@@ -234,23 +234,34 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
 
     // ---- pass 1: m/d of student (a) and teacher (b) together ----
     MD ma{-CUDART_INF_F, 0.f}, mb{-CUDART_INF_F, 0.f};
-    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
-      float xs[N], xt[N];
-      V::load(zs + i * N, xs);
-      V::load(zt + i * N, xt);
-#pragma unroll
-      for (int k = 0; k < N; ++k) {
-        xs[k] = __fmul_rn(xs[k], c);
-        xt[k] = __fmul_rn(xt[k], c);
+    if (a.stats_s != nullptr) {
+      // the logits GEMM already folded each 256-column tile of this row
+      const float2* ps = a.stats_s + r * a.ntiles;
+      const float2* pt = a.stats_t + r * a.ntiles;
+      for (int64_t i = threadIdx.x; i < a.ntiles; i += blockDim.x) {
+        const float2 u = ps[i], w2 = pt[i];
+        ma = md_combine(ma, MD{u.x, u.y});
+        mb = md_combine(mb, MD{w2.x, w2.y});
       }
-      md_fold<N>(ma, xs);
-      md_fold<N>(mb, xt);
-    }
-    for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-      float xs[1] = {__fmul_rn(V::one(zs + j), c)};
-      float xt[1] = {__fmul_rn(V::one(zt + j), c)};
-      md_fold<1>(ma, xs);
-      md_fold<1>(mb, xt);
+    } else {
+      for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+        float xs[N], xt[N];
+        V::load(zs + i * N, xs);
+        V::load(zt + i * N, xt);
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          xs[k] = __fmul_rn(xs[k], c);
+          xt[k] = __fmul_rn(xt[k], c);
+        }
+        md_fold<N>(ma, xs);
+        md_fold<N>(mb, xt);
+      }
+      for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
+        float xs[1] = {__fmul_rn(V::one(zs + j), c)};
+        float xt[1] = {__fmul_rn(V::one(zt + j), c)};
+        md_fold<1>(ma, xs);
+        md_fold<1>(mb, xt);
+      }
     }
     const MD ra = block_md(ma, sh_md);
     const MD rb = block_md(mb, sh_md);
@@ -290,7 +301,9 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
 
     // ---- pass 3: dlogits in place over the student logits ----
     const float scale = w * a.inv_temperature;
-    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+    // walk the row backwards: the lines pass 2 read last are the likeliest to
+    // still be in L2
+    for (int64_t i = nvec - 1 - threadIdx.x; i >= 0; i -= blockDim.x) {
       float xs[N], xt[N];
       V::load(zs + i * N, xs);
       V::load(zt + i * N, xt);
@@ -375,7 +388,9 @@ __global__ void k_scale(T* p, int64_t n, const float* gp) {
 
 template <typename T, int BRANCH>
 cudaError_t launch_rows_t(const JsdRowArgs& a, cudaStream_t st) {
-  const int64_t grid = a.rows < (int64_t)num_sms() * 4 ? a.rows : (int64_t)num_sms() * 4;
+  // One row in flight per SM keeps the rows between pass 2 and pass 3 small
+  // enough for L2 (148 rows of 2 x 256 KB at V = 128256 in bf16).
+  const int64_t grid = a.rows < (int64_t)num_sms() ? a.rows : (int64_t)num_sms();
   k_jsd_rows<T, BRANCH><<<(unsigned)grid, kRowThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
