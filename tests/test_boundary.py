@@ -58,7 +58,12 @@ def test_plan_single_chunk_and_memory_accounting(L):
     assert plan.chunk_rows == 8192 and plan.num_chunks == 1 and plan.ld == 128256
     assert plan.logits_bytes == 2 * 8192 * 128256 * 2
     assert plan.workspace_bytes >= plan.logits_bytes + 8192 * 4
-    assert plan.workspace_bytes - plan.logits_bytes < 64 * 1024 + 8192 * 4 * 2
+    # beyond the logits: loss_1d (BT*4), the pass-1 partials of both models
+    # (8 bytes per row per 256-column tile each) and alignment
+    partials = 2 * 8192 * (-(-128256 // 256)) * 8
+    assert plan.stats_bytes >= partials + 8192 * 4
+    extra = plan.workspace_bytes - plan.logits_bytes
+    assert partials + 8192 * 4 <= extra < partials + 8192 * 4 + 4096
     # ld is padded to a multiple of 8 elements (16-byte rows in bf16)
     plan = L.fljsd_plan(L.make_problem(64, 128, 128, 1000, "fp32"), 0)
     assert plan.ld == 1000
