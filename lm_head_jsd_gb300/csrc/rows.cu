@@ -132,12 +132,15 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
 }
 
 // ---- per-element branch arithmetic (log2 units) -----------------------------
-// Y2 = log2 P (teacher) and d = X2 - Y2 = log2(Q / P), where X2 = log2 Q is the
-// student log-prob. Working from d keeps the generalized branch accurate when
-// P and Q are close: with u = 2^d = Q / P and s = beta + (1 - beta) u = M / P,
-//   X2 - log2 M = d - log2 s,   Y2 - log2 M = -log2 s,
-// so no error of the absolute P or Q enters the log term, and Q = P u makes
-// the pair consistent. BRANCH 0: forward KL(P||Q); 1: reverse KL(Q||P);
+// Inputs per element: Y2 = log2 P (teacher) and d = X2 - Y2 = log2(Q / P),
+// X2 = log2 Q (student). The generalized branch works from the larger of the
+// two probabilities, big = 2^max(X2, Y2), and the ratio e = 2^-|d| <= 1:
+//   small = big * e,  M / big = w1 * e + w0  (w1, w0 = 1-beta, beta when
+//   d <= 0, else beta, 1-beta),  lg = log2(M / big),
+//   X2 - log2 M = min(d, 0) - lg,  Y2 - log2 M = -max(d, 0) - lg.
+// Nothing overflows for any d, P and Q come out consistent, and when P and Q
+// are close the log term is computed from their ratio, not from two rounded
+// absolute values. BRANCH 0: forward KL(P||Q); 1: reverse KL(Q||P);
 // 2: generalized JSD. PREC selects the accurate library exp2f/log2f (fp32
 // inputs) instead of the ex2/lg2 units (bf16 inputs).
 template <bool PREC>
@@ -151,24 +154,41 @@ __device__ __forceinline__ float plog2(float x) {
   return lg2(x);
 }
 
+// Generalized-branch terms of one element: Q, P*beta, and the two log ratios.
+template <bool PREC>
+__device__ __forceinline__ void gen_terms(float Y2, float d, float beta, float omb, float& Q,
+                                          float& bP, float& xm, float& ym) {
+  const bool neg = d <= 0.f;
+  const float e = pexp2<PREC>(-fabsf(d));
+  const float big = pexp2<PREC>(Y2 + fmaxf(d, 0.f));
+  const float small = big * e;
+  const float lg = plog2<PREC>(fmaf(neg ? omb : beta, e, neg ? beta : omb));
+  Q = neg ? small : big;
+  bP = beta * (neg ? big : small);
+  xm = fminf(d, 0.f) - lg;
+  ym = -fmaxf(d, 0.f) - lg;
+}
+
 // Per-element loss (log2 units, loss / ln 2) and, for the generalized branch,
 // the log-prob gradient dX (also / ln 2). A tie (d == 0) contributes exactly 0.
 template <int BRANCH, bool PREC>
 __device__ __forceinline__ void elem_loss(float Y2, float d, float beta, float omb,
                                           float& ell, float& g) {
-  ell = 0.f;
-  g = 0.f;
-  if (d == 0.f) return;
   if (BRANCH == 0) {
     ell = -pexp2<PREC>(Y2) * d;  // P (Y - X)
+    g = 0.f;
   } else if (BRANCH == 1) {
     ell = pexp2<PREC>(Y2 + d) * d;  // Q (X - Y)
+    g = 0.f;
   } else {
-    const float P = pexp2<PREC>(Y2);
-    const float u = pexp2<PREC>(d);
-    const float ls = plog2<PREC>(fmaf(omb, u, beta));
-    g = omb * (P * u) * (d - ls);
-    ell = g - beta * P * ls;
+    float Q, bP, xm, ym;
+    gen_terms<PREC>(Y2, d, beta, omb, Q, bP, xm, ym);
+    g = omb * Q * xm;
+    ell = fmaf(bP, ym, g);
+  }
+  if (d == 0.f) {
+    ell = 0.f;
+    g = 0.f;
   }
 }
 
@@ -180,15 +200,14 @@ __device__ __forceinline__ float elem_grad(float Y2, float d, float beta, float 
   const float ln2 = 0.6931471805599453f;
   if (BRANCH == 0) {
     if (d == 0.f) return 0.f;
-    return pexp2<PREC>(Y2) * (pexp2<PREC>(d) - 1.f);  // Q - P
+    return pexp2<PREC>(Y2 + d) - pexp2<PREC>(Y2);  // Q - P
   } else if (BRANCH == 1) {
     return pexp2<PREC>(Y2 + d) * (ln2 * (d - L2));  // Q (X - Y - L)
   } else {
-    const float P = pexp2<PREC>(Y2);
-    const float u = pexp2<PREC>(d);
-    const float Q = P * u;
-    const float g = (d == 0.f) ? 0.f : omb * Q * (d - plog2<PREC>(fmaf(omb, u, beta)));
-    return ln2 * (g - Q * S2);
+    float Q, bP, xm, ym;
+    gen_terms<PREC>(Y2, d, beta, omb, Q, bP, xm, ym);
+    const float g = (d == 0.f) ? 0.f : omb * Q * xm;
+    return ln2 * fmaf(-Q, S2, g);
   }
 }
 
@@ -277,9 +296,8 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       V::load(zt + i * N, xt);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const float as = __fmul_rn(xs[k], c), bs = __fmul_rn(xt[k], c);
-        const float Y2 = __fsub_rn(bs, lse_b);
-        const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
+        const float Y2 = __fmaf_rn(xt[k], c, -lse_b);
+        const float d = __fmaf_rn(__fsub_rn(xs[k], xt[k]), c, -dlse);
         float ell, g;
         elem_loss<BRANCH, PREC>(Y2, d, beta, omb, ell, g);
         acc.x += ell;
@@ -287,9 +305,9 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       }
     }
     for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-      const float as = __fmul_rn(V::one(zs + j), c), bs = __fmul_rn(V::one(zt + j), c);
-      const float Y2 = __fsub_rn(bs, lse_b);
-      const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
+      const float xsj = V::one(zs + j), xtj = V::one(zt + j);
+      const float Y2 = __fmaf_rn(xtj, c, -lse_b);
+      const float d = __fmaf_rn(__fsub_rn(xsj, xtj), c, -dlse);
       float ell, g;
       elem_loss<BRANCH, PREC>(Y2, d, beta, omb, ell, g);
       acc.x += ell;
@@ -309,17 +327,16 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       V::load(zt + i * N, xt);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const float as = __fmul_rn(xs[k], c), bs = __fmul_rn(xt[k], c);
-        const float Y2 = __fsub_rn(bs, lse_b);
-        const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
+        const float Y2 = __fmaf_rn(xt[k], c, -lse_b);
+        const float d = __fmaf_rn(__fsub_rn(xs[k], xt[k]), c, -dlse);
         xs[k] = elem_grad<BRANCH, PREC>(Y2, d, beta, omb, L2, S2) * scale;
       }
       V::store(zs + i * N, xs);
     }
     for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-      const float as = __fmul_rn(V::one(zs + j), c), bs = __fmul_rn(V::one(zt + j), c);
-      const float Y2 = __fsub_rn(bs, lse_b);
-      const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
+      const float xsj = V::one(zs + j), xtj = V::one(zt + j);
+      const float Y2 = __fmaf_rn(xtj, c, -lse_b);
+      const float d = __fmaf_rn(__fsub_rn(xsj, xtj), c, -dlse);
       V::put(zs + j, elem_grad<BRANCH, PREC>(Y2, d, beta, omb, L2, S2) * scale);
     }
     __syncthreads();

@@ -220,3 +220,20 @@ def test_deterministic():
     b = run_gpu(*inputs, beta=0.5)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("beta", BETAS)
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+def test_extreme_temperature(beta, dt):
+    """T = 0.02 multiplies the logits by 50: log-probabilities fall hundreds of
+    units below zero, probabilities underflow and the ratio Q/P leaves the fp32
+    range, which must give finite, correct results. In bf16 the logits' own
+    rounding error is magnified 50 times, so there the oracle rounds the logits
+    and dlogits to bf16 as the kernels store them (its diagnostic mode)."""
+    w = jsd_inputs.custom("extremeT", 51, 96, 64, 3000, dt, ignore_frac=0.1)
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    for red in ("none", "sum"):
+        out = run_gpu(*inputs, beta=beta, temperature=0.02, reduction=red)
+        ref = _oracle(inputs, beta=beta, temperature=0.02, reduction=red,
+                      emulate_rounding=(dt == "bf16"))
+        compare(out, ref, dt, f"T=0.02 beta={beta} {dt} {red}")
