@@ -132,6 +132,10 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
 }
 
 // ---- per-element branch arithmetic (log2 units) -----------------------------
+// The callers form a = z * log2(e)/T rounded once (as the GEMM epilogue did
+// for the row statistics), Y2 = b - lse_b and d = (a - b) - (lse_a - lse_b):
+// a row whose student and teacher log-probabilities are equal (equal logits,
+// or V == 1) then gets d == 0 exactly, which is what the tie rule tests.
 // Inputs per element: Y2 = log2 P (teacher) and d = X2 - Y2 = log2(Q / P),
 // X2 = log2 Q (student). The generalized branch works from the larger of the
 // two probabilities, big = 2^max(X2, Y2), and the ratio e = 2^-|d| <= 1:
@@ -296,8 +300,9 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       V::load(zt + i * N, xt);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const float Y2 = __fmaf_rn(xt[k], c, -lse_b);
-        const float d = __fmaf_rn(__fsub_rn(xs[k], xt[k]), c, -dlse);
+        const float as = __fmul_rn(xs[k], c), bs = __fmul_rn(xt[k], c);
+        const float Y2 = __fsub_rn(bs, lse_b);
+        const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
         float ell, g;
         elem_loss<BRANCH, PREC>(Y2, d, beta, omb, ell, g);
         acc.x += ell;
@@ -305,9 +310,9 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       }
     }
     for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-      const float xsj = V::one(zs + j), xtj = V::one(zt + j);
-      const float Y2 = __fmaf_rn(xtj, c, -lse_b);
-      const float d = __fmaf_rn(__fsub_rn(xsj, xtj), c, -dlse);
+      const float as = __fmul_rn(V::one(zs + j), c), bs = __fmul_rn(V::one(zt + j), c);
+      const float Y2 = __fsub_rn(bs, lse_b);
+      const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
       float ell, g;
       elem_loss<BRANCH, PREC>(Y2, d, beta, omb, ell, g);
       acc.x += ell;
@@ -327,16 +332,17 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       V::load(zt + i * N, xt);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const float Y2 = __fmaf_rn(xt[k], c, -lse_b);
-        const float d = __fmaf_rn(__fsub_rn(xs[k], xt[k]), c, -dlse);
+        const float as = __fmul_rn(xs[k], c), bs = __fmul_rn(xt[k], c);
+        const float Y2 = __fsub_rn(bs, lse_b);
+        const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
         xs[k] = elem_grad<BRANCH, PREC>(Y2, d, beta, omb, L2, S2) * scale;
       }
       V::store(zs + i * N, xs);
     }
     for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-      const float xsj = V::one(zs + j), xtj = V::one(zt + j);
-      const float Y2 = __fmaf_rn(xtj, c, -lse_b);
-      const float d = __fmaf_rn(__fsub_rn(xsj, xtj), c, -dlse);
+      const float as = __fmul_rn(V::one(zs + j), c), bs = __fmul_rn(V::one(zt + j), c);
+      const float Y2 = __fsub_rn(bs, lse_b);
+      const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
       V::put(zs + j, elem_grad<BRANCH, PREC>(Y2, d, beta, omb, L2, S2) * scale);
     }
     __syncthreads();
