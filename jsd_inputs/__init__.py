@@ -39,6 +39,7 @@ class Workload:
     ignore_frac: float = 0.0
     tie: str = "none"  # "none" | "self" (X_t=X_s, W_t=W_s) | "padded"
     pad_frac: float = 0.0  # fraction of trailing vocab rows zeroed in W_s and W_t
+    spike: int = 0  # > 0: the first `spike` tokens get a shared logit offset (below)
 
     @property
     def torch_dtype(self):
@@ -109,6 +110,22 @@ def make_inputs(w: Workload, device: str = "cpu"):
         first = w.v - int(round(w.pad_frac * w.v))
         w_s[first:] = 0.0
         w_t[first:] = 0.0
+    if w.spike > 0:
+        # Hidden column 0 is 1 in both models and the first `spike` vocab rows
+        # carry a weight of 8 there and 1% of the random weights elsewhere
+        # (the teacher's with an independent 1% perturbation), so these tokens
+        # lead both distributions by about 4 logit units or more and stay close to
+        # each other, while every other token keeps an N(0, 1) logit that
+        # differs between the models.
+        k = w.spike
+        x_s[:, 0] = 1.0
+        w_s[:k] *= 0.01
+        w_s[:k, 0] = 8.0
+        if w.tie != "self":
+            if x_t is not x_s:
+                x_t[:, 0] = 1.0
+            w_t[:k] = w_s[:k] + 0.01 * _randn((k, w.h_t), 1.0 / math.sqrt(w.h_t), gen, device)
+            w_t[:k, 0] = 8.0
     dt = w.torch_dtype
     x_s, w_s = x_s.to(dt), w_s.to(dt)
     if w.tie == "self":
