@@ -378,12 +378,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             st_d = (st_m == -INFINITY) ? 0.f : st_d * ex2f_approx(st_m - cm);
             st_m = cm;
           }
+          // exponent = x * scale - max with the exact product rounded once, so
+          // that large scaled logits (small T) keep their precision near the max
           float acc_d = 0.f;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             if (col0 + e < p.n)
               acc_d += ex2f_approx(
-                  __fmul_rn(__bfloat162float(__float2bfloat16_rn(v[e])), p.stats_scale) - st_m);
+                  __fmaf_rn(__bfloat162float(__float2bfloat16_rn(v[e])), p.stats_scale, -st_m));
           }
           st_d += acc_d;
         }

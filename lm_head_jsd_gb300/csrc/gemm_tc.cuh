@@ -23,7 +23,8 @@ struct TcGemmArgs {
   int* status;           // device word that receives FLJSD_ERR_TIMEOUT, or null
   // Optional row statistics of the stored output (requires accumulate == 0):
   // for row r and n-tile j (TC_TILE_N columns), stats[r * ceil(n / TC_TILE_N) + j]
-  // = (max_x, sum 2^(x - max_x)) over x = bf16(D[r, col]) * stats_scale.
+  // = (m, sum 2^(x - m)) over x = bf16(D[r, col]) * stats_scale, where m is the
+  // largest rounded product and each x - m is formed from the exact product.
   float2* stats;
   float stats_scale;
 };

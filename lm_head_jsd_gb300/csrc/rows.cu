@@ -81,19 +81,21 @@ __device__ __forceinline__ MD md_combine(MD a, MD b) {
   return MD{m, d};
 }
 
-// Fold a group of values (already in log2 units) into a running (m, d).
+// Fold a group of logits z into a running (m, d) of x = z * c (log2 units):
+// m is the largest rounded product, and each x - m comes from the exact
+// product rounded once (the same rule as the GEMM epilogue's partials).
 template <int N>
-__device__ __forceinline__ void md_fold(MD& s, const float (&x)[N]) {
-  float vm = x[0];
+__device__ __forceinline__ void md_fold(MD& s, const float (&z)[N], float c) {
+  float vm = __fmul_rn(z[0], c);
 #pragma unroll
-  for (int i = 1; i < N; ++i) vm = fmaxf(vm, x[i]);
+  for (int i = 1; i < N; ++i) vm = fmaxf(vm, __fmul_rn(z[i], c));
   if (vm > s.m) {
     s.d = (s.m == -CUDART_INF_F) ? 0.f : s.d * ex2(s.m - vm);
     s.m = vm;
   }
   float acc = 0.f;
 #pragma unroll
-  for (int i = 0; i < N; ++i) acc += ex2(x[i] - s.m);
+  for (int i = 0; i < N; ++i) acc += ex2(__fmaf_rn(z[i], c, -s.m));
   s.d += acc;
 }
 
@@ -132,10 +134,9 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
 }
 
 // ---- per-element branch arithmetic (log2 units) -----------------------------
-// The callers form a = z * log2(e)/T rounded once (as the GEMM epilogue did
-// for the row statistics), Y2 = b - lse_b and d = (a - b) - (lse_a - lse_b):
-// a row whose student and teacher log-probabilities are equal (equal logits,
-// or V == 1) then gets d == 0 exactly, which is what the tie rule tests.
+// The callers form X2 = fma(z_s, c, -m_a) - log2 d_a and Y2 likewise, and
+// d = X2 - Y2: equal student and teacher rows give d == 0 exactly, which is
+// what the tie rule tests.
 // Inputs per element: Y2 = log2 P (teacher) and d = X2 - Y2 = log2(Q / P),
 // X2 = log2 Q (student). The generalized branch works from the larger of the
 // two probabilities, big = 2^max(X2, Y2), and the ratio e = 2^-|d| <= 1:
@@ -271,26 +272,26 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
         float xs[N], xt[N];
         V::load(zs + i * N, xs);
         V::load(zt + i * N, xt);
-#pragma unroll
-        for (int k = 0; k < N; ++k) {
-          xs[k] = __fmul_rn(xs[k], c);
-          xt[k] = __fmul_rn(xt[k], c);
-        }
-        md_fold<N>(ma, xs);
-        md_fold<N>(mb, xt);
+        md_fold<N>(ma, xs, c);
+        md_fold<N>(mb, xt, c);
       }
       for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-        float xs[1] = {__fmul_rn(V::one(zs + j), c)};
-        float xt[1] = {__fmul_rn(V::one(zt + j), c)};
-        md_fold<1>(ma, xs);
-        md_fold<1>(mb, xt);
+        float xs[1] = {V::one(zs + j)};
+        float xt[1] = {V::one(zt + j)};
+        md_fold<1>(ma, xs, c);
+        md_fold<1>(mb, xt, c);
       }
     }
     const MD ra = block_md(ma, sh_md);
     const MD rb = block_md(mb, sh_md);
-    const float lse_a = ra.m + plog2<PREC>(ra.d);  // log2-sum-exp2 of the scaled student logits
-    const float lse_b = rb.m + plog2<PREC>(rb.d);
-    const float dlse = __fsub_rn(lse_a, lse_b);
+    // log2 Q_j = z_j * c - m_a - log2 d_a, formed as fma(z, c, -m) - log2 d so
+    // that the exact product is rounded once relative to the row maximum.
+    // A one-element row has log-prob 0 whatever its logit.
+    const bool single = (a.v == 1);
+    const float ma_ = single ? 0.f : ra.m, mb_ = single ? 0.f : rb.m;
+    const float lda = single ? 0.f : plog2<PREC>(ra.d);
+    const float ldb = single ? 0.f : plog2<PREC>(rb.d);
+    const float cz = single ? 0.f : c;
 
     // ---- pass 2: loss and dX_sum ----
     float2 acc = make_float2(0.f, 0.f);
@@ -300,9 +301,8 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       V::load(zt + i * N, xt);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const float as = __fmul_rn(xs[k], c), bs = __fmul_rn(xt[k], c);
-        const float Y2 = __fsub_rn(bs, lse_b);
-        const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
+        const float Y2 = __fsub_rn(__fmaf_rn(xt[k], cz, -mb_), ldb);
+        const float d = __fsub_rn(__fsub_rn(__fmaf_rn(xs[k], cz, -ma_), lda), Y2);
         float ell, g;
         elem_loss<BRANCH, PREC>(Y2, d, beta, omb, ell, g);
         acc.x += ell;
@@ -310,9 +310,8 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       }
     }
     for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-      const float as = __fmul_rn(V::one(zs + j), c), bs = __fmul_rn(V::one(zt + j), c);
-      const float Y2 = __fsub_rn(bs, lse_b);
-      const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
+      const float Y2 = __fsub_rn(__fmaf_rn(V::one(zt + j), cz, -mb_), ldb);
+      const float d = __fsub_rn(__fsub_rn(__fmaf_rn(V::one(zs + j), cz, -ma_), lda), Y2);
       float ell, g;
       elem_loss<BRANCH, PREC>(Y2, d, beta, omb, ell, g);
       acc.x += ell;
@@ -332,17 +331,15 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
       V::load(zt + i * N, xt);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const float as = __fmul_rn(xs[k], c), bs = __fmul_rn(xt[k], c);
-        const float Y2 = __fsub_rn(bs, lse_b);
-        const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
+        const float Y2 = __fsub_rn(__fmaf_rn(xt[k], cz, -mb_), ldb);
+        const float d = __fsub_rn(__fsub_rn(__fmaf_rn(xs[k], cz, -ma_), lda), Y2);
         xs[k] = elem_grad<BRANCH, PREC>(Y2, d, beta, omb, L2, S2) * scale;
       }
       V::store(zs + i * N, xs);
     }
     for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-      const float as = __fmul_rn(V::one(zs + j), c), bs = __fmul_rn(V::one(zt + j), c);
-      const float Y2 = __fsub_rn(bs, lse_b);
-      const float d = __fsub_rn(__fsub_rn(as, bs), dlse);
+      const float Y2 = __fsub_rn(__fmaf_rn(V::one(zt + j), cz, -mb_), ldb);
+      const float d = __fsub_rn(__fsub_rn(__fmaf_rn(V::one(zs + j), cz, -ma_), lda), Y2);
       V::put(zs + j, elem_grad<BRANCH, PREC>(Y2, d, beta, omb, L2, S2) * scale);
     }
     __syncthreads();
