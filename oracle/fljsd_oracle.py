@@ -77,6 +77,13 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     return out.astype(np.float64)
 
 
+def _store_round(x: np.ndarray, mode) -> np.ndarray:
+    """Round to the storage dtype named by ``mode`` (True/"bf16" or "fp32")."""
+    if mode == "fp32":
+        return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+    return bf16_round(x)
+
+
 # ---------------------------------------------------------------------------
 # the two logits GEMMs
 # ---------------------------------------------------------------------------
@@ -187,9 +194,12 @@ def fljsd_ref(x_s, w_s, x_t, w_t, labels=None, *, beta: float = 0.5,
     is independent of the others except through the valid-row count n.
     grad_weight is the sum over blocks of dz^T . X_s (PR 1429, "Summary").
 
-    With ``emulate_rounding`` the logits and dlogits are rounded to bf16 as the
-    bf16 kernels store them (PR 1352, "Open questions" 1 and "Details"); it is
-    a diagnostic, not the definition.
+    With ``emulate_rounding`` the logits and dlogits are rounded to the input
+    dtype as the kernels store them (PR 1352, "Open questions" 1: the GEMM
+    output keeps the input dtype; "Details": dlogits overwrite the logits
+    buffer): True or "bf16" rounds to bfloat16, "fp32" to float32. It is a
+    diagnostic for cases where 1/T magnifies the storage rounding, not the
+    definition.
 
     Returns (loss, grad_input, grad_weight): loss is a float for sum, mean and
     batchmean, and a [BT] array for none.
@@ -208,7 +218,7 @@ def fljsd_ref(x_s, w_s, x_t, w_t, labels=None, *, beta: float = 0.5,
             zs = logits(x_s[r0:r1], w_s)
             zt = logits(x_t[r0:r1], w_t)
             if emulate_rounding:
-                zs, zt = bf16_round(zs), bf16_round(zt)
+                zs, zt = _store_round(zs, emulate_rounding), _store_round(zt, emulate_rounding)
             yield r0, r1, zs, zt
 
     return _from_logit_blocks(blocks(), x_s, w_s, labels, beta, temperature, reduction,
@@ -249,7 +259,7 @@ def _from_logit_blocks(blocks, x_s, w_s, labels, beta, temperature, reduction, i
         dz = dA * (w[r0:r1] / temperature)[:, None]
         dz[~vb] = 0.0
         if emulate_rounding:
-            dz = bf16_round(dz)
+            dz = _store_round(dz, emulate_rounding)
         grad_input[r0:r1] = dz @ w_s
         grad_weight += dz.T @ x_s[r0:r1]
     if reduction == "none":

@@ -360,3 +360,22 @@ def test_rows_reference_matches_full_reference_rows():
                                 row_scale=np.ones(3))
     np.testing.assert_allclose(L, rows[idx], rtol=1e-13)
     np.testing.assert_allclose(gir, gi[idx], rtol=1e-12)
+
+
+def test_storage_rounding_modes():
+    """The diagnostic rounding: fp32 mode equals NumPy's float32 cast of the
+    logits; bf16 mode equals the bf16 rounding pinned above."""
+    from oracle import logits
+
+    x_s, w_s, x_t, w_t = _problem(19, bt=5, h=6, v=40)
+    for mode, rnd in (("fp32", lambda z: z.astype(np.float32).astype(np.float64)),
+                      ("bf16", bf16_round)):
+        got = fljsd_ref(x_s, w_s, x_t, w_t, beta=0.3, temperature=0.5, reduction="sum",
+                        emulate_rounding=mode)
+        from oracle import fljsd_from_logits
+
+        ref = fljsd_from_logits(rnd(logits(x_s, w_s)), rnd(logits(x_t, w_t)), x_s, w_s, beta=0.3,
+                                temperature=0.5, reduction="sum")
+        assert got[0] == pytest.approx(ref[0], rel=1e-12)
+        # dlogits are rounded in the mode too, so the gradients differ slightly
+        assert np.linalg.norm(got[1] - ref[1]) <= 1e-2 * np.linalg.norm(ref[1])

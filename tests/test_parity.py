@@ -229,15 +229,16 @@ def test_extreme_temperature(beta, dt):
     distributions (so they are not one-hot), while the other tokens' student and
     teacher log-probabilities differ by far more than 128 in log2 units: the
     ratio Q/P leaves the fp32 range and probabilities underflow, which must give
-    finite, correct results. In bf16 the logits' own rounding error is
-    magnified 50 times, so there the oracle rounds the logits and dlogits to
-    bf16 as the kernels store them (its diagnostic mode)."""
+    finite, correct results. The logits' own storage rounding (to the input
+    dtype) is magnified 50 times, so here the oracle rounds its logits and
+    dlogits to the input dtype as the kernels store them (its diagnostic
+    mode)."""
     w = jsd_inputs.custom("extremeT", 51, 96, 64, 3000, dt, ignore_frac=0.1, spike=16)
     inputs = jsd_inputs.make_inputs(w, "cpu")
     for red in ("none", "sum"):
         out = run_gpu(*inputs, beta=beta, temperature=0.02, reduction=red)
         ref = _oracle(inputs, beta=beta, temperature=0.02, reduction=red,
-                      emulate_rounding=(dt == "bf16"))
+                      emulate_rounding=dt)
         compare(out, ref, dt, f"T=0.02 beta={beta} {dt} {red}")
 
 
