@@ -47,9 +47,11 @@ def run_gpu(x_s, w_s, x_t, w_t, labels=None, *, beta=0.5, temperature=1.0,
     return loss, gi, gw
 
 
-def compare(gpu, ref, dtype: str, what=""):
-    """gpu = (loss, grad_input, grad_weight) tensors; ref = oracle outputs."""
-    tol_loss, tol_grad = TOL[dtype]
+def compare(gpu, ref, dtype: str, what="", scale_tol: float = 1.0):
+    """gpu = (loss, grad_input, grad_weight) tensors; ref = oracle outputs.
+    ``scale_tol`` widens both tolerances (only for stress cases whose caller
+    derives the factor from the arithmetic)."""
+    tol_loss, tol_grad = (t * scale_tol for t in TOL[dtype])
     loss, gi, gw = (f64(t) for t in gpu)
     rl, rgi, rgw = ref
     rl = np.atleast_1d(np.asarray(rl, dtype=np.float64))
