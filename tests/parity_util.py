@@ -26,10 +26,18 @@ def rel_fro(got, ref) -> float:
 
 
 def assert_zeros_where_ref_zero(got, ref, what):
+    """Exact zeros of the method -- ignored rows, fully tied rows, an all-zero
+    result -- must come out as exact zeros. They show as oracle rows (of a
+    vector: elements) that are entirely 0.0; an isolated 0.0 inside a nonzero
+    row is a numerical cancellation, not a zero of the method."""
     got = np.asarray(got)
     ref = np.asarray(ref)
-    mask = ref == 0.0
-    bad = int(np.count_nonzero(got[mask] != 0.0))
+    if ref.ndim == 1:
+        mask = ref == 0.0
+        bad = int(np.count_nonzero(got[mask] != 0.0))
+    else:
+        zero_rows = np.all(ref == 0.0, axis=1)
+        bad = int(np.count_nonzero(got[zero_rows] != 0.0))
     assert bad == 0, f"{what}: {bad} elements are nonzero where the oracle is exactly 0"
 
 

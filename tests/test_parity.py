@@ -252,18 +252,26 @@ def test_extreme_temperature(beta, dt):
 
 
 @pytest.mark.parametrize("beta", BETAS)
-def test_saturated_rows_stay_finite(beta):
+def test_saturated_rows(beta):
     """Independent student and teacher at T = 0.02: every row is one-hot at
-    different tokens, the loss is at its bound h(beta) and the true gradient is
-    about 1e-15 of the terms it is computed from -- below what any fp32
-    evaluation resolves (the float64 oracle is at its own noise floor there).
-    The loss must still match, and the gradients must be finite and tiny."""
+    different tokens. For the KL endpoints the loss is large and the gradient
+    (Q - P)/T is O(1/T): compared with the fp32 tolerances times 1/T (the fp32
+    GEMM's error is magnified by 1/T). For the generalized JSD the loss sits at
+    its bound h(beta) and the true gradient is about 1e-15 of the terms it is
+    computed from -- below what any fp32 evaluation resolves (the float64
+    oracle is at its own noise floor there): the loss must still match, and the
+    gradients must be finite and tiny."""
+    T = 0.02
     w = jsd_inputs.custom("saturated", 52, 96, 64, 3000, "fp32", ignore_frac=0.1)
     inputs = jsd_inputs.make_inputs(w, "cpu")
-    loss, gi, gw = run_gpu(*inputs, beta=beta, temperature=0.02, reduction="none")
-    ref = _oracle(inputs, beta=beta, temperature=0.02, reduction="none")
+    out = run_gpu(*inputs, beta=beta, temperature=T, reduction="none")
+    ref = _oracle(inputs, beta=beta, temperature=T, reduction="none")
+    if beta in (0.0, 1.0):
+        compare(out, ref, "fp32", f"saturated beta={beta}", scale_tol=1.0 / T)
+        return
+    loss, gi, gw = out
     assert rel_fro(f64(loss), ref[0]) <= 1e-5
     for g in (gi, gw):
         assert torch.all(torch.isfinite(g))
-    # gradient terms are O(1/T) per element; fp32 leaves them at the 1e-4 level
+    # the terms are O(1/T) per element; fp32 leaves their difference near 1e-5
     assert float(gi.abs().max()) < 1e-2 and float(gw.abs().max()) < 1e-2
