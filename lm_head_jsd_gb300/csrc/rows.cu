@@ -174,6 +174,22 @@ __device__ __forceinline__ void gen_terms(float Y2, float d, float beta, float o
   ym = -fmaxf(d, 0.f) - lg;
 }
 
+// Generalized-branch terms, direct form (bf16 inputs): P = 2^Y2, Q = 2^X2 and
+// log2 M from their mixture. Both probabilities are <= 1, so nothing
+// overflows; M is clamped to the smallest normal float so that rows whose P
+// and Q both underflow give finite (zero-weighted) log terms. Cheaper than the
+// ratio form, and accurate well inside the bf16 tolerances.
+__device__ __forceinline__ void gen_terms_direct(float Y2, float d, float beta, float omb,
+                                                 float& Q, float& bP, float& xm, float& ym) {
+  const float X2 = Y2 + d;
+  Q = ex2(X2);
+  const float P = ex2(Y2);
+  bP = beta * P;
+  const float lM = lg2(fmaxf(fmaf(omb, Q, bP), 1.17549435e-38f));
+  xm = X2 - lM;
+  ym = Y2 - lM;
+}
+
 // Per-element loss (log2 units, loss / ln 2) and, for the generalized branch,
 // the log-prob gradient dX (also / ln 2). A tie (d == 0) contributes exactly 0.
 template <int BRANCH, bool PREC>
@@ -187,7 +203,10 @@ __device__ __forceinline__ void elem_loss(float Y2, float d, float beta, float o
     g = 0.f;
   } else {
     float Q, bP, xm, ym;
-    gen_terms<PREC>(Y2, d, beta, omb, Q, bP, xm, ym);
+    if (PREC)
+      gen_terms<PREC>(Y2, d, beta, omb, Q, bP, xm, ym);
+    else
+      gen_terms_direct(Y2, d, beta, omb, Q, bP, xm, ym);
     g = omb * Q * xm;
     ell = fmaf(bP, ym, g);
   }
@@ -210,7 +229,10 @@ __device__ __forceinline__ float elem_grad(float Y2, float d, float beta, float 
     return pexp2<PREC>(Y2 + d) * (ln2 * (d - L2));  // Q (X - Y - L)
   } else {
     float Q, bP, xm, ym;
-    gen_terms<PREC>(Y2, d, beta, omb, Q, bP, xm, ym);
+    if (PREC)
+      gen_terms<PREC>(Y2, d, beta, omb, Q, bP, xm, ym);
+    else
+      gen_terms_direct(Y2, d, beta, omb, Q, bP, xm, ym);
     const float g = (d == 0.f) ? 0.f : omb * Q * xm;
     return ln2 * fmaf(-Q, S2, g);
   }
