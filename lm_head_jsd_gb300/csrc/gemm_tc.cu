@@ -191,6 +191,7 @@ struct KParams {
   float stats_scale;   // x = bf16(value) * stats_scale
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
   int raster_n_fastest;
+  int group_m;  // m-blocks per band in the grouped order
   int accumulate;
   int* status;
 };
@@ -230,13 +231,21 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = cb->tmem_base;
 
+  // Tile order. n-fastest: all n-blocks of a few m-blocks run together (used
+  // when B is small and A streams). Grouped: bands of group_m m-blocks; inside
+  // a band the m-blocks vary fastest and the band walks every n-block, so the
+  // band's slice of A stays in L2 while B streams through once per band.
   auto tile_coords = [&](int t, int& mb, int& nb) {
     if (p.raster_n_fastest) {
       nb = t % p.num_n_blocks;
       mb = t / p.num_n_blocks;
     } else {
-      mb = t % p.num_m_blocks;
-      nb = t / p.num_m_blocks;
+      const int band = t / (p.group_m * p.num_n_blocks);
+      const int m0 = band * p.group_m;
+      const int gm = min(p.group_m, p.num_m_blocks - m0);
+      const int r = t - band * p.group_m * p.num_n_blocks;
+      mb = m0 + r % gm;
+      nb = r / gm;
     }
   };
 
@@ -519,6 +528,15 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
   p.num_tiles = (int)tiles;
   p.raster_n_fastest = g.raster_n_fastest;
+  // band of A rows whose K extent stays around 16 MB (at least one m-block)
+  {
+    const int64_t band_bytes = 16ll << 20;
+    const int64_t per_mblock = (int64_t)BM * g.k * 2;
+    int64_t gm = per_mblock > 0 ? band_bytes / per_mblock : 1;
+    if (gm < 1) gm = 1;
+    if (gm > p.num_m_blocks) gm = p.num_m_blocks;
+    p.group_m = (int)gm;
+  }
   p.accumulate = g.accumulate;
   p.status = g.status;
   p.stats = g.stats;
