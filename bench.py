@@ -46,6 +46,30 @@ def _peaks():
                 "source": "fallback"}
 
 
+def _profiled_traffic(kernel: str, source: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the kernel's source has changed since the counters were taken."""
+    import glob
+    import hashlib
+
+    src = os.path.join(ROOT, "lm_head_jsd_gb300", "csrc", source)
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    for path in glob.glob(os.path.join(ROOT, "profiles", "dram_traffic_*.md")):
+        vals = {}
+        for line in open(path):
+            parts = line.split()
+            if len(parts) == 3 and parts[0] == kernel:
+                vals[parts[1].rstrip(":")] = parts[2]
+        key = "traffic_bytes_per_launch_avg" if "traffic_bytes_per_launch_avg" in vals else \
+            "traffic_bytes_per_launch"
+        if vals.get("source_sha256_16") == h and key in vals:
+            return int(vals[key])
+    return None
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -285,7 +309,9 @@ def main():
                          f"{run.plan.logits_bytes / 1e9:.1f} GB)"},
         "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (4 launches per chunk)",
                      "achieved": round(achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak_tc, 4), "traffic": None,
+                     "frac": round(achieved / peak_tc, 4),
+                     "traffic": _profiled_traffic("k_gemm_tc", "gemm_tc.cu")
+                     if w.name == "headline" else None,
                      "peak_kind": f"bf16 sustained ({peaks['source']})"},
         "roofline_step": {"flop": flop_step, "roofline_ms": round(step_roof_ms, 3),
                           "frac": round(step_roof_ms / ms_step, 4),
@@ -293,7 +319,9 @@ def main():
         "roofline_jsd": {"bound": "hbm", "achieved": round(jsd_gbs, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(jsd_gbs / peaks["hbm_gbs"], 4),
-                         "algorithmic_bytes": "3*C*V*s per launch"},
+                         "algorithmic_bytes": "3*C*V*s per launch",
+                         "traffic": _profiled_traffic("k_jsd_rows", "rows.cu")
+                         if w.name == "headline" else None},
         "kernel_ms_per_step": {k: round(v[0] / max(steps_traced, 1), 4) for k, v in kinds.items()},
         "gpu_launches": launches,
         "clocks": clk,
