@@ -89,7 +89,22 @@ typedef struct {
   float temperature;    /* > 0 and finite; logits are divided by it once */
   int64_t ignore_index; /* label value of rows that are skipped (Liger: -100) */
   int64_t chunk_rows;   /* rows per chunk; 0 lets fljsd_plan choose */
+  int32_t flags;        /* FLJSD_FLAG_* bits, 0 for the pages' behaviour */
+  int32_t reserved;     /* must be 0 */
 } fljsd_problem;
+
+/* Opt-in behaviours (none of them is the pages' default).
+ * FLJSD_FLAG_T2: multiply the loss and both gradients by T^2 (Hinton et al.
+ *   2015); the pages divide by T once and leave this to the caller
+ *   ("[Perf] Fuse log-softmax into fused_linear_jsd kernel", Open questions 2).
+ * FLJSD_FLAG_ACCUM_FP32: with bf16 inputs and more than one chunk, accumulate
+ *   grad_weight across chunks in an fp32 buffer inside the workspace
+ *   (V * h_s * 4 bytes) and round it to bf16 once after the last chunk, as
+ *   the accum_dtype=float32 option of "perf(flce): write the weight-gradient
+ *   product directly into grad_weight" (PR 1429) does; without it every chunk
+ *   after the first rounds the running sum to bf16. */
+#define FLJSD_FLAG_T2 1
+#define FLJSD_FLAG_ACCUM_FP32 2
 
 typedef struct {
   int64_t chunk_rows;     /* C: rows of one chunk */

@@ -33,7 +33,12 @@ class fljsd_problem(ctypes.Structure):
     _fields_ = [("bt", ctypes.c_int64), ("h_s", ctypes.c_int64), ("h_t", ctypes.c_int64),
                 ("v", ctypes.c_int64), ("dtype", ctypes.c_int32), ("reduction", ctypes.c_int32),
                 ("beta", ctypes.c_float), ("temperature", ctypes.c_float),
-                ("ignore_index", ctypes.c_int64), ("chunk_rows", ctypes.c_int64)]
+                ("ignore_index", ctypes.c_int64), ("chunk_rows", ctypes.c_int64),
+                ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+FLJSD_FLAG_T2 = 1
+FLJSD_FLAG_ACCUM_FP32 = 2
 
 
 class fljsd_plan_t(ctypes.Structure):
@@ -106,10 +111,12 @@ def _stream(stream) -> int | None:
 
 
 def make_problem(bt, h_s, h_t, v, dtype="bf16", reduction="batchmean", beta=0.5,
-                 temperature=1.0, ignore_index=-100, chunk_rows=0) -> fljsd_problem:
+                 temperature=1.0, ignore_index=-100, chunk_rows=0, t2_scale=False,
+                 accum_fp32=False) -> fljsd_problem:
+    flags = (FLJSD_FLAG_T2 if t2_scale else 0) | (FLJSD_FLAG_ACCUM_FP32 if accum_fp32 else 0)
     return fljsd_problem(bt, h_s, h_t, v, DTYPES[dtype] if isinstance(dtype, str) else dtype,
                          REDUCTIONS[reduction] if isinstance(reduction, str) else reduction,
-                         beta, temperature, ignore_index, chunk_rows)
+                         beta, temperature, ignore_index, chunk_rows, flags, 0)
 
 
 def fljsd_status_string(status: int) -> str:

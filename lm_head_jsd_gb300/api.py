@@ -33,14 +33,14 @@ class FusedLinearJSD:
 
     def __init__(self, bt, h_s, h_t, v, dtype=torch.bfloat16, *, beta=0.5, temperature=1.0,
                  reduction="batchmean", ignore_index=-100, chunk_rows=0, device="cuda",
-                 free_hbm_bytes=None):
+                 free_hbm_bytes=None, t2_scale=False, accum_fp32=False):
         self.device = torch.device(device)
         if self.device.type == "cuda" and self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
         self.dtype = dtype
         self.reduction = reduction
         self.problem = make_problem(bt, h_s, h_t, v, _DT[dtype], reduction, beta, temperature,
-                                    ignore_index, chunk_rows)
+                                    ignore_index, chunk_rows, t2_scale, accum_fp32)
         if free_hbm_bytes is None:
             free_hbm_bytes = torch.cuda.mem_get_info(self.device)[0]
         self.plan = fljsd_plan(self.problem, int(free_hbm_bytes))

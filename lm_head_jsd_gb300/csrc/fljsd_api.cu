@@ -82,7 +82,8 @@ inline size_t dtype_size(int dt) { return dt == FLJSD_BF16 ? 2 : 4; }
 
 struct Layout {
   int64_t ld, ntiles;
-  size_t zs, zt, stats_s, stats_t, loss_rows, misc, total, logits_bytes, stats_bytes;
+  size_t zs, zt, stats_s, stats_t, loss_rows, misc, acc32, total, logits_bytes, stats_bytes;
+  bool use_acc32;
 };
 
 Layout layout_for(const fljsd_problem& p, int64_t chunk_rows) {
@@ -99,7 +100,10 @@ Layout layout_for(const fljsd_problem& p, int64_t chunk_rows) {
   L.stats_t = L.stats_s + sbytes;
   L.loss_rows = L.stats_t + sbytes;
   L.misc = L.loss_rows + align_up((size_t)p.bt * sizeof(float));
-  L.total = L.misc + kAlign;
+  // fp32 grad_weight accumulator: only when it changes anything
+  L.use_acc32 = (p.flags & FLJSD_FLAG_ACCUM_FP32) && p.dtype == FLJSD_BF16 && chunk_rows < p.bt;
+  L.acc32 = L.misc + kAlign;
+  L.total = L.acc32 + (L.use_acc32 ? align_up((size_t)p.v * (size_t)p.h_s * sizeof(float)) : 0);
   L.logits_bytes = 2 * (size_t)chunk_rows * (size_t)L.ld * s;
   L.stats_bytes = 2 * sbytes + align_up((size_t)p.bt * sizeof(float)) + kAlign;
   return L;
@@ -114,6 +118,8 @@ fljsd_status check_problem(const fljsd_problem* p) {
   if (!(p->beta >= 0.f && p->beta <= 1.f)) return FLJSD_ERR_INVALID_ARG;  // also rejects NaN
   if (!(p->temperature > 0.f) || !std::isfinite(p->temperature)) return FLJSD_ERR_INVALID_ARG;
   if (p->chunk_rows < 0) return FLJSD_ERR_INVALID_ARG;
+  if ((p->flags & ~(FLJSD_FLAG_T2 | FLJSD_FLAG_ACCUM_FP32)) != 0 || p->reserved != 0)
+    return FLJSD_ERR_INVALID_ARG;
   // grid limits of the kernels (rows of a chunk and vocabulary tiles)
   if (p->v > (int64_t)1 << 30 || p->bt > (int64_t)1 << 30) return FLJSD_ERR_UNSUPPORTED;
   if (p->h_s > (int64_t)1 << 20 || p->h_t > (int64_t)1 << 20) return FLJSD_ERR_UNSUPPORTED;
@@ -133,13 +139,13 @@ cudaError_t run_gemm(int dtype, int kind, const void* a, int64_t lda, int a_mn, 
                      int64_t ldb, int b_mn, void* d, int64_t ldd, int64_t m, int64_t n, int64_t k,
                      int accumulate, int raster_n_fastest, int* status, cudaStream_t st,
                      float2* stats = nullptr, float stats_scale = 0.f,
-                     bool* stats_done = nullptr) {
+                     bool* stats_done = nullptr, float* d32 = nullptr, int finalize = 0) {
   if (stats_done) *stats_done = false;
   if (m <= 0 || n <= 0) return cudaSuccess;
   cudaError_t e;
   trace_begin(kind, st);
-  TcGemmArgs t{a,        lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, raster_n_fastest,
-               status,   stats, stats_scale};
+  TcGemmArgs t{a,      lda,   a_mn,        b,   ldb,     b_mn, d, ldd, m, n, k, accumulate,
+               raster_n_fastest, status, stats, stats_scale, d32, finalize};
   if (dtype == FLJSD_BF16 && tc_gemm_supported(t)) {
     e = launch_gemm_tc(t, st);
     if (stats_done) *stats_done = stats != nullptr;
@@ -148,6 +154,7 @@ cudaError_t run_gemm(int dtype, int kind, const void* a, int64_t lda, int a_mn, 
     g.a = a; g.sam = a_mn ? 1 : lda; g.sak = a_mn ? lda : 1;
     g.b = b; g.sbn = b_mn ? 1 : ldb; g.sbk = b_mn ? ldb : 1;
     g.c = d; g.ldc = ldd; g.m = m; g.n = n; g.k = k; g.accumulate = accumulate;
+    g.c32 = d32; g.finalize = finalize;
     e = launch_gemm_simt(dtype, g, st);
   }
   trace_end(kind, st);
@@ -242,6 +249,7 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
   int* status = n_valid + 1;  // device status word, reset by the row-count kernel
   float2* stats_s = reinterpret_cast<float2*>(ws + L.stats_s);
   float2* stats_t = reinterpret_cast<float2*>(ws + L.stats_t);
+  float* acc32 = reinterpret_cast<float*>(ws + L.acc32);
   const size_t s = dtype_size(p->dtype);
 
   cudaError_t e = launch_count_valid(labels, p->bt, p->ignore_index, n_valid, stream);
@@ -271,6 +279,7 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
     ra.row_grad = p->reduction == FLJSD_RED_NONE ? row_grad : nullptr;
     ra.n_valid = n_valid; ra.loss_rows = loss_rows; ra.reduction = p->reduction;
     ra.beta = p->beta; ra.inv_temperature = 1.0f / p->temperature; ra.scale_log2 = c2;
+    ra.loss_scale = (p->flags & FLJSD_FLAG_T2) ? p->temperature * p->temperature : 1.0f;
     // the partials are used only when both GEMMs produced them (same code path
     // for student and teacher, so equal logits give equal statistics)
     ra.stats_s = (st_s && st_t) ? stats_s : nullptr;
@@ -287,8 +296,16 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
 
     // grad_weight (+)= dZ^T . X_s: both operands stored with the chunk rows as
     // the outer dimension (M-major A, N-major B); the first chunk overwrites
-    e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_WEIGHT, zs, L.ld, 1, xs_c, p->h_s, 1,
-                 grad_weight, p->h_s, p->v, p->h_s, rows, chunk > 0 ? 1 : 0, 1, status, stream);
+    const bool last = (r0 + rows >= p->bt);
+    if (L.use_acc32) {
+      // fp32 accumulator across chunks, rounded to the input dtype once
+      e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_WEIGHT, zs, L.ld, 1, xs_c, p->h_s, 1,
+                   grad_weight, p->h_s, p->v, p->h_s, rows, chunk > 0 ? 1 : 0, 1, status, stream,
+                   nullptr, 0.f, nullptr, acc32, last ? 1 : 0);
+    } else {
+      e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_WEIGHT, zs, L.ld, 1, xs_c, p->h_s, 1,
+                   grad_weight, p->h_s, p->v, p->h_s, rows, chunk > 0 ? 1 : 0, 1, status, stream);
+    }
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
   }
 
@@ -336,7 +353,8 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
   if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1) || (accumulate != 0 && accumulate != 1))
     return FLJSD_ERR_INVALID_ARG;
   if (lda < (a_mn ? m : k) || ldb < (b_mn ? n : k) || ldd < n) return FLJSD_ERR_INVALID_ARG;
-  TcGemmArgs t{a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, 1, status, nullptr, 0.f};
+  TcGemmArgs t{a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, 1, status, nullptr, 0.f,
+               nullptr, 0};
   if (!tc_gemm_supported(t)) return FLJSD_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   trace_begin(FLJSD_KERNEL_SMALL, stream);

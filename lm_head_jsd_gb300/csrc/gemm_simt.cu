@@ -84,8 +84,15 @@ __global__ void __launch_bounds__(THREADS) k_gemm_simt(GemmArgs g) {
       if (n >= g.n) continue;
       T* out = C + m * g.ldc + n;
       float v = acc[i][j];
-      if (g.accumulate) v += ld_f<T>(out);
-      *out = to_t<T>(v);
+      if (g.c32 != nullptr) {
+        float* o32 = g.c32 + m * g.ldc + n;
+        if (g.accumulate || g.finalize) v += *o32;
+        if (g.finalize) *out = to_t<T>(v);
+        else *o32 = v;
+      } else {
+        if (g.accumulate) v += ld_f<T>(out);
+        *out = to_t<T>(v);
+      }
     }
   }
 }

@@ -193,6 +193,8 @@ struct KParams {
   int raster_n_fastest;
   int group_m;  // m-blocks per band in the grouped order
   int accumulate;
+  float* d32;    // optional fp32 accumulator with row stride ldd (see TcGemmArgs)
+  int finalize;
   int* status;
 };
 
@@ -406,7 +408,35 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = v[q * 8 + e];
           __nv_bfloat16* dst = drow + col;
-          if (col + 8 <= p.n) {
+          if (p.d32 != nullptr) {
+            // fp32 accumulator: D32 (+)= product, or on the last pass
+            // D = round(D32 + product)
+            float* s32 = p.d32 + row * p.ldd + col;
+            const int ne = (col + 8 <= p.n) ? 8 : (int)(p.n - col);
+            if (ne == 8) {
+              if (p.accumulate || p.finalize) {
+                const float4 a0 = reinterpret_cast<const float4*>(s32)[0];
+                const float4 a1 = reinterpret_cast<const float4*>(s32)[1];
+                x[0] += a0.x; x[1] += a0.y; x[2] += a0.z; x[3] += a0.w;
+                x[4] += a1.x; x[5] += a1.y; x[6] += a1.z; x[7] += a1.w;
+              }
+              if (p.finalize) {
+                *reinterpret_cast<uint4*>(dst) =
+                    make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                               pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+              } else {
+                reinterpret_cast<float4*>(s32)[0] = make_float4(x[0], x[1], x[2], x[3]);
+                reinterpret_cast<float4*>(s32)[1] = make_float4(x[4], x[5], x[6], x[7]);
+              }
+            } else {
+              for (int e = 0; e < ne; ++e) {
+                float y = x[e];
+                if (p.accumulate || p.finalize) y += s32[e];
+                if (p.finalize) dst[e] = __float2bfloat16_rn(y);
+                else s32[e] = y;
+              }
+            }
+          } else if (col + 8 <= p.n) {
             uint4* d4 = reinterpret_cast<uint4*>(dst);
             if (p.accumulate) {
               const uint4 o = *d4;
@@ -538,6 +568,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
     p.group_m = (int)gm;
   }
   p.accumulate = g.accumulate;
+  p.d32 = g.d32;
+  p.finalize = g.finalize;
   p.status = g.status;
   p.stats = g.stats;
   p.stats_scale = g.stats_scale;

@@ -27,6 +27,11 @@ struct TcGemmArgs {
   // largest rounded product and each x - m is formed from the exact product.
   float2* stats;
   float stats_scale;
+  // Optional fp32 accumulator [m x ldd] (16-byte aligned). With d32 set the
+  // product goes to d32 (added to it when accumulate == 1) and D is not
+  // touched, unless finalize == 1: then D = round(d32 + product).
+  float* d32;
+  int finalize;
 };
 
 constexpr int TC_TILE_N = 256;

@@ -43,6 +43,7 @@ struct JsdRowArgs {
   float beta;
   float inv_temperature;
   float scale_log2;  // log2(e) / T, the same constant the GEMM epilogue used
+  float loss_scale;  // 1, or T^2 with FLJSD_FLAG_T2 (loss and gradients)
 };
 
 cudaError_t launch_count_valid(const int64_t* labels, int64_t bt, int64_t ignore_index,
@@ -62,6 +63,8 @@ struct GemmArgs {
   void* c; int64_t ldc;
   int64_t m, n, k;
   int accumulate;  // 0: C = A.B^T ; 1: C = C + A.B^T (fp32 add, one rounding)
+  float* c32;      // optional fp32 accumulator [m x ldc]: as TcGemmArgs::d32
+  int finalize;
 };
 
 // CUDA-core FFMA GEMM for any layout (fp32 path, and shapes the tensor-core

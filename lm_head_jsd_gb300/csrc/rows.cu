@@ -341,10 +341,10 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
     }
     const float2 tot = block_sum2(acc, sh_s);
     const float L2 = tot.x, S2 = tot.y;  // row loss and dX_sum, / ln 2
-    if (threadIdx.x == 0) a.loss_rows[grow] = 0.6931471805599453f * L2;
+    if (threadIdx.x == 0) a.loss_rows[grow] = 0.6931471805599453f * L2 * a.loss_scale;
 
     // ---- pass 3: dlogits in place over the student logits ----
-    const float scale = w * a.inv_temperature;
+    const float scale = w * a.inv_temperature * a.loss_scale;
     // walk the row backwards: the lines pass 2 read last are the likeliest to
     // still be in L2
     for (int64_t i = nvec - 1 - threadIdx.x; i >= 0; i -= blockDim.x) {

@@ -187,7 +187,7 @@ def row_weights(labels, bt: int, v: int, reduction: str, ignore_index: int = -10
 def fljsd_ref(x_s, w_s, x_t, w_t, labels=None, *, beta: float = 0.5,
               temperature: float = 1.0, reduction: str = "batchmean",
               ignore_index: int = -100, row_grad=None, emulate_rounding: bool = False,
-              block_rows: int = 256):
+              block_rows: int = 256, t2_scale: bool = False):
     """Loss, grad_input (d/dX_s) and grad_weight (d/dW_s) of the fused-linear JSD.
 
     Rows are processed in blocks of ``block_rows`` only to bound memory; each row
@@ -200,6 +200,10 @@ def fljsd_ref(x_s, w_s, x_t, w_t, labels=None, *, beta: float = 0.5,
     buffer): True or "bf16" rounds to bfloat16, "fp32" to float32. It is a
     diagnostic for cases where 1/T magnifies the storage rounding, not the
     definition.
+
+    ``t2_scale`` multiplies the loss and both gradients by T^2 (the opt-in
+    Hinton et al. 2015 scaling that PR 1352, "Open questions" 2, discusses; off
+    by default, as on the pages).
 
     Returns (loss, grad_input, grad_weight): loss is a float for sum, mean and
     batchmean, and a [BT] array for none.
@@ -221,8 +225,12 @@ def fljsd_ref(x_s, w_s, x_t, w_t, labels=None, *, beta: float = 0.5,
                 zs, zt = _store_round(zs, emulate_rounding), _store_round(zt, emulate_rounding)
             yield r0, r1, zs, zt
 
-    return _from_logit_blocks(blocks(), x_s, w_s, labels, beta, temperature, reduction,
-                              ignore_index, row_grad, emulate_rounding)
+    out = _from_logit_blocks(blocks(), x_s, w_s, labels, beta, temperature, reduction,
+                             ignore_index, row_grad, emulate_rounding)
+    if t2_scale:
+        t2 = temperature * temperature
+        out = (out[0] * t2, out[1] * t2, out[2] * t2)
+    return out
 
 
 def fljsd_from_logits(z_s, z_t, x_s, w_s, labels=None, *, beta: float = 0.5,

@@ -379,3 +379,23 @@ def test_storage_rounding_modes():
         assert got[0] == pytest.approx(ref[0], rel=1e-12)
         # dlogits are rounded in the mode too, so the gradients differ slightly
         assert np.linalg.norm(got[1] - ref[1]) <= 1e-2 * np.linalg.norm(ref[1])
+
+
+def test_t2_scaling_reaches_the_high_temperature_limit():
+    """Hinton et al. 2015, section 2.1: at high temperature the soft-target
+    gradient (Q - P)/T approaches (z_s - z_t)/(N T^2) for zero-mean logits, so
+    the T^2-scaled gradient approaches (z_s - z_t)/N, independent of T."""
+    r = _rng(20)
+    v = 17
+    zs = r.standard_normal((3, v)); zs -= zs.mean(axis=1, keepdims=True)
+    zt = r.standard_normal((3, v)); zt -= zt.mean(axis=1, keepdims=True)
+    eye = np.eye(v)
+    T = 1e4
+    _, gi, _ = fljsd_ref(zs, eye, zt, eye, beta=0.0, temperature=T, reduction="sum",
+                         t2_scale=True)
+    np.testing.assert_allclose(gi, (zs - zt) / v, rtol=2e-3, atol=1e-7)
+    loss1, gi1, gw1 = fljsd_ref(zs, eye, zt, eye, beta=0.3, temperature=2.0, reduction="sum")
+    loss2, gi2, gw2 = fljsd_ref(zs, eye, zt, eye, beta=0.3, temperature=2.0, reduction="sum",
+                                t2_scale=True)
+    assert loss2 == pytest.approx(4.0 * loss1, rel=1e-14)
+    np.testing.assert_allclose(gi2, 4.0 * gi1, rtol=1e-14)

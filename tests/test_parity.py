@@ -275,3 +275,37 @@ def test_saturated_rows(beta):
         assert torch.all(torch.isfinite(g))
     # the terms are O(1/T) per element; fp32 leaves their difference near 1e-5
     assert float(gi.abs().max()) < 1e-2 and float(gw.abs().max()) < 1e-2
+
+
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+@pytest.mark.parametrize("beta", (0.0, 0.5, 1.0))
+def test_t2_scaling_flag(dt, beta):
+    w = jsd_inputs.custom("t2", 61, 130, 64, 2000, dt, ignore_frac=0.1)
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    from lm_head_jsd_gb300 import FusedLinearJSD
+
+    x_s, w_s, x_t, w_t, labels = (t.cuda() for t in inputs)
+    for red in ("batchmean", "none"):
+        run = FusedLinearJSD(130, 64, 64, 2000, w.torch_dtype, beta=beta, temperature=3.0,
+                             reduction=red, t2_scale=True)
+        out = run.forward(x_s, w_s, x_t, w_t, labels)
+        torch.cuda.synchronize()
+        ref = _oracle(inputs, beta=beta, temperature=3.0, reduction=red, t2_scale=True)
+        compare(out, ref, dt, f"T^2 beta={beta} {red}")
+
+
+@pytest.mark.parametrize("chunk", [1, 7, 64])
+def test_fp32_grad_weight_accumulation(chunk):
+    """With the fp32 accumulator, hundreds of chunks stay within the bf16
+    tolerance (without it, 300 one-row chunks drift to ~1.8e-2)."""
+    from lm_head_jsd_gb300 import FusedLinearJSD
+
+    w = jsd_inputs.custom("chunks", 21, 300, 64, 5000, "bf16", ignore_frac=0.1)
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    ref = _oracle(inputs, beta=0.5, temperature=1.0, reduction="batchmean")
+    x_s, w_s, x_t, w_t, labels = (t.cuda() for t in inputs)
+    run = FusedLinearJSD(300, 64, 64, 5000, torch.bfloat16, chunk_rows=chunk, accum_fp32=True)
+    assert run.plan.workspace_bytes >= 5000 * 64 * 4
+    out = run.forward(x_s, w_s, x_t, w_t, labels)
+    torch.cuda.synchronize()
+    compare(out, ref, "bf16", f"accum fp32 chunk={chunk}")
