@@ -393,7 +393,9 @@ def test_t2_scaling_reaches_the_high_temperature_limit():
     T = 1e4
     _, gi, _ = fljsd_ref(zs, eye, zt, eye, beta=0.0, temperature=T, reduction="sum",
                          t2_scale=True)
-    np.testing.assert_allclose(gi, (zs - zt) / v, rtol=2e-3, atol=1e-7)
+    ref = (zs - zt) / v
+    # the next term of the expansion is O(|z| / T) relative
+    assert np.linalg.norm(gi - ref) <= 1e-3 * np.linalg.norm(ref)
     loss1, gi1, gw1 = fljsd_ref(zs, eye, zt, eye, beta=0.3, temperature=2.0, reduction="sum")
     loss2, gi2, gw2 = fljsd_ref(zs, eye, zt, eye, beta=0.3, temperature=2.0, reduction="sum",
                                 t2_scale=True)
