@@ -224,6 +224,46 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
                              int64_t n, int64_t k, int32_t accumulate, int32_t* status,
                              fljsd_stream_t stream);
 
+/*
+ * Distances over given distributions (no GEMM). Both take [rows x v] row-major
+ * tensors of `dtype`, optional int64 labels [rows] (rows whose label equals
+ * ignore_index give loss 0 and gradient 0; n = the other rows), a reduction
+ * as for fljsd_forward (none / sum / mean = / (n v) / batchmean = / n), and a
+ * device workspace of fljsd_rows_workspace_bytes(rows) bytes. They return the
+ * gradient for an upstream gradient of 1 (fljsd_scale applies another).
+ *
+ * fljsd_jsd_logspace -- the generalized JSD on log-probabilities, the public
+ * contract of Liger's _jsd_kernel ("[Perf] Fuse log-softmax into
+ * fused_linear_jsd kernel", PR 1352, Open questions 3): input = X = log Q
+ * (student), target = Y = log P (teacher); per element beta*P*(Y - log M) +
+ * (1-beta)*Q*(X - log M) with M = beta*P + (1-beta)*Q, forward KL P*(Y - X) at
+ * beta == 0, reverse KL Q*(X - Y) at beta == 1; ties (X == Y) contribute 0.
+ * grad_input = d loss / d X element by element (inputs are not renormalised,
+ * so no softmax Jacobian): (1-beta)*Q*(X - log M), -P at beta == 0,
+ * Q*(X - Y + 1) at beta == 1, times the reduction weight. loss: [1], or [rows]
+ * for reduction none.
+ *
+ * fljsd_tvd -- total variation distance with the tie fix of "Fix TVD
+ * gradient at p == q" (PR 1374, Summary): per element 0.5*|p - q|, gradient
+ * in p = 0.5 * sign(p - q) * (reduction weight) with sign(0) = 0. loss: [1],
+ * or [rows x v] fp32 per element for reduction none.
+ *
+ * fljsd_scale -- x *= *grad_output in place (device fp32 scalar), skipped on
+ * the device when it is 1: the backward of the two functions above.
+ */
+size_t fljsd_rows_workspace_bytes(int64_t rows);
+fljsd_status fljsd_jsd_logspace(int64_t rows, int64_t v, int32_t dtype, float beta,
+                                int32_t reduction, int64_t ignore_index, const void* input,
+                                const void* target, const int64_t* labels, float* loss,
+                                void* grad_input, void* workspace, size_t workspace_bytes,
+                                fljsd_stream_t stream);
+fljsd_status fljsd_tvd(int64_t rows, int64_t v, int32_t dtype, int32_t reduction,
+                       int64_t ignore_index, const void* p, const void* q, const int64_t* labels,
+                       float* loss, void* grad_p, void* workspace, size_t workspace_bytes,
+                       fljsd_stream_t stream);
+fljsd_status fljsd_scale(int32_t dtype, void* x, int64_t n, const float* grad_output,
+                         fljsd_stream_t stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 const char* fljsd_status_string(fljsd_status status);
 

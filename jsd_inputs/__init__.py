@@ -143,3 +143,29 @@ def custom(name: str, seed: int, bt: int, h_s: int, v: int, dtype: str = "bf16",
            h_t: int | None = None, **kw) -> Workload:
     """A workload of arbitrary shape with the same recipe (for small and odd shapes)."""
     return Workload(name, seed, bt, h_s, h_s if h_t is None else h_t, v, dtype, **kw)
+
+
+def make_distributions(rows: int, v: int, dtype: str, seed: int, *, logspace: bool,
+                       scale: float = 2.0, tied_rows: int = 0, tied_frac: float = 0.0,
+                       ignore_frac: float = 0.0, device: str = "cpu"):
+    """Two [rows x V] distributions for the distance paths: softmax (or
+    log_softmax when ``logspace``) of seeded N(0, scale^2) scores, computed in
+    float32 and cast to the dtype. The first ``tied_rows`` rows of the second
+    tensor equal the first's; in the other rows the trailing ``tied_frac`` of
+    the vocabulary is copied from the first tensor (padded-vocabulary style
+    ties). Returns (a, b, labels)."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    sa = _randn((rows, v), scale, g, device)
+    sb = _randn((rows, v), scale, g, device)
+    f = torch.log_softmax if logspace else torch.softmax
+    a = f(sa, dim=-1).to(torch.float32 if dtype == "fp32" else torch.bfloat16)
+    b = f(sb, dim=-1).to(a.dtype)
+    if tied_rows:
+        b[:tied_rows] = a[:tied_rows]
+    if tied_frac > 0.0:
+        k = v - int(round(tied_frac * v))
+        b[tied_rows:, k:] = a[tied_rows:, k:]
+    labels = make_labels(rows, v, ignore_frac, seed)
+    if labels is not None:
+        labels = labels.to(device)
+    return a.contiguous(), b.contiguous(), labels

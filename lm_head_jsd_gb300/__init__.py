@@ -10,6 +10,10 @@ from ._lib import (  # noqa: F401
     fljsd_forward,
     fljsd_forward_noalloc,
     fljsd_gemm_bf16,
+    fljsd_jsd_logspace,
+    fljsd_rows_workspace_bytes,
+    fljsd_scale,
+    fljsd_tvd,
     fljsd_launch_count,
     fljsd_launch_count_reset,
     fljsd_plan,
@@ -20,6 +24,6 @@ from ._lib import (  # noqa: F401
     fljsd_workspace_status,
     make_problem,
 )
-from .api import FusedLinearJSD, fused_linear_jsd  # noqa: F401
+from .api import FusedLinearJSD, fused_linear_jsd, jsd_logspace, tvd  # noqa: F401
 
 LIB_PATH = _lib.LIB_PATH

@@ -72,6 +72,17 @@ def _load():
                                     ctypes.c_int32, P, ctypes.c_int64, ctypes.c_int64,
                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, P, P]
     lib.fljsd_gemm_bf16.restype = ctypes.c_int
+    lib.fljsd_rows_workspace_bytes.argtypes = [ctypes.c_int64]
+    lib.fljsd_rows_workspace_bytes.restype = ctypes.c_size_t
+    lib.fljsd_jsd_logspace.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                       ctypes.c_float, ctypes.c_int32, ctypes.c_int64, P, P, P,
+                                       P, P, P, ctypes.c_size_t, P]
+    lib.fljsd_jsd_logspace.restype = ctypes.c_int
+    lib.fljsd_tvd.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                              ctypes.c_int64, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.fljsd_tvd.restype = ctypes.c_int
+    lib.fljsd_scale.argtypes = [ctypes.c_int32, P, ctypes.c_int64, P, P]
+    lib.fljsd_scale.restype = ctypes.c_int
     lib.fljsd_status_string.argtypes = [ctypes.c_int]
     lib.fljsd_status_string.restype = ctypes.c_char_p
     lib.fljsd_launch_count.argtypes = []
@@ -180,6 +191,51 @@ def fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate=0, s
                              accumulate, _ptr(status), _stream(stream))
     if check and st != FLJSD_OK:
         raise FljsdError(st, "fljsd_gemm_bf16")
+    return st
+
+
+def _dt(dtype):
+    return DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+
+
+def _red(reduction):
+    return REDUCTIONS[reduction] if isinstance(reduction, str) else int(reduction)
+
+
+def fljsd_rows_workspace_bytes(rows: int) -> int:
+    return lib.fljsd_rows_workspace_bytes(rows)
+
+
+def fljsd_jsd_logspace(rows, v, dtype, beta, reduction, ignore_index, input, target, labels,
+                       loss, grad_input, workspace, workspace_bytes=None, stream=None,
+                       check=True) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = lib.fljsd_jsd_logspace(rows, v, _dt(dtype), beta, _red(reduction), ignore_index,
+                                _ptr(input), _ptr(target), _ptr(labels), _ptr(loss),
+                                _ptr(grad_input), _ptr(workspace), workspace_bytes,
+                                _stream(stream))
+    if check and st != FLJSD_OK:
+        raise FljsdError(st, "fljsd_jsd_logspace")
+    return st
+
+
+def fljsd_tvd(rows, v, dtype, reduction, ignore_index, p, q, labels, loss, grad_p, workspace,
+              workspace_bytes=None, stream=None, check=True) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = lib.fljsd_tvd(rows, v, _dt(dtype), _red(reduction), ignore_index, _ptr(p), _ptr(q),
+                       _ptr(labels), _ptr(loss), _ptr(grad_p), _ptr(workspace), workspace_bytes,
+                       _stream(stream))
+    if check and st != FLJSD_OK:
+        raise FljsdError(st, "fljsd_tvd")
+    return st
+
+
+def fljsd_scale(dtype, x, n, grad_output, stream=None, check=True) -> int:
+    st = lib.fljsd_scale(_dt(dtype), _ptr(x), n, _ptr(grad_output), _stream(stream))
+    if check and st != FLJSD_OK:
+        raise FljsdError(st, "fljsd_scale")
     return st
 
 

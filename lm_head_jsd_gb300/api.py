@@ -123,4 +123,62 @@ def fused_linear_jsd(x_s, w_s, x_t, w_t, labels=None, *, beta=0.5, temperature=1
                                          int(chunk_rows))
 
 
-__all__ = ["FusedLinearJSD", "fused_linear_jsd", "_lib"]
+def _dist_call(kind, x, y, labels, reduction, ignore_index, beta=0.5):
+    if x.shape != y.shape or x.dim() != 2:
+        raise ValueError("expected two [rows x V] tensors of the same shape")
+    _check("x", x, None, x.device)
+    _check("y", y, x.dtype, x.device)
+    if labels is not None:
+        _check("labels", labels, torch.int64, x.device, (x.shape[0],))
+    rows, v = x.shape
+    if reduction == "none":
+        loss = torch.empty((rows, v) if kind == "tvd" else (rows,), dtype=torch.float32,
+                           device=x.device)
+    else:
+        loss = torch.empty(1, dtype=torch.float32, device=x.device)
+    grad = torch.empty_like(x)
+    ws = torch.empty(_lib.fljsd_rows_workspace_bytes(rows), dtype=torch.uint8, device=x.device)
+    if kind == "tvd":
+        _lib.fljsd_tvd(rows, v, _DT[x.dtype], reduction, ignore_index, x, y, labels, loss, grad, ws)
+    else:
+        _lib.fljsd_jsd_logspace(rows, v, _DT[x.dtype], beta, reduction, ignore_index, x, y,
+                                labels, loss, grad, ws)
+    return loss, grad
+
+
+class _DistFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, kind, x, y, labels, reduction, ignore_index, beta):
+        loss, grad = _dist_call(kind, x.detach().contiguous(), y.detach().contiguous(),
+                                None if labels is None else labels.contiguous(), reduction,
+                                ignore_index, beta)
+        ctx.save_for_backward(grad)
+        ctx.reduction = reduction
+        ctx.dtype = x.dtype
+        return loss if reduction == "none" else loss.reshape(())
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        (grad,) = ctx.saved_tensors
+        if ctx.reduction == "none":
+            raise NotImplementedError("backward through reduction='none' is not provided")
+        g = grad_out.detach().to(torch.float32).reshape(1).contiguous()
+        _lib.fljsd_scale(_DT[ctx.dtype], grad, grad.numel(), g)
+        return None, grad, None, None, None, None, None
+
+
+def jsd_logspace(input, target, labels=None, *, beta=0.5, reduction="batchmean",
+                 ignore_index=-100):
+    """Generalized JSD between given log-probabilities (input = log Q, student;
+    target = log P, teacher), differentiable in input."""
+    return _DistFunction.apply("jsd", input, target, labels, reduction, int(ignore_index),
+                               float(beta))
+
+
+def tvd(p, q, labels=None, *, reduction="batchmean", ignore_index=-100):
+    """Total variation distance 0.5 * sum |p - q| (zero gradient at ties),
+    differentiable in p."""
+    return _DistFunction.apply("tvd", p, q, labels, reduction, int(ignore_index), 0.0)
+
+
+__all__ = ["FusedLinearJSD", "fused_linear_jsd", "jsd_logspace", "tvd", "_lib"]

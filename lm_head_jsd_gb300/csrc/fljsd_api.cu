@@ -363,6 +363,84 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
   return e == cudaSuccess ? FLJSD_OK : FLJSD_ERR_CUDA;
 }
 
+size_t fljsd_rows_workspace_bytes(int64_t rows) {
+  if (rows <= 0) return 0;
+  return align_up((size_t)rows * sizeof(float)) + kAlign;
+}
+
+static fljsd_status dist_common(int64_t rows, int64_t v, int32_t dtype, int32_t reduction,
+                                const void* x, const void* y, float* loss, void* grad,
+                                void* workspace, size_t workspace_bytes) {
+  if (rows <= 0 || v <= 0 || rows > (int64_t)1 << 31 || v > (int64_t)1 << 31)
+    return FLJSD_ERR_INVALID_ARG;
+  if (dtype != FLJSD_F32 && dtype != FLJSD_BF16) return FLJSD_ERR_INVALID_ARG;
+  if (reduction < FLJSD_RED_NONE || reduction > FLJSD_RED_BATCHMEAN) return FLJSD_ERR_INVALID_ARG;
+  if (!x || !y || !loss || !grad || !workspace) return FLJSD_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(grad) || !aligned16(workspace) ||
+      ((uintptr_t)loss & 3u))
+    return FLJSD_ERR_INVALID_ARG;
+  if (workspace_bytes < fljsd_rows_workspace_bytes(rows)) return FLJSD_ERR_WORKSPACE;
+  return FLJSD_OK;
+}
+
+fljsd_status fljsd_jsd_logspace(int64_t rows, int64_t v, int32_t dtype, float beta,
+                                int32_t reduction, int64_t ignore_index, const void* input,
+                                const void* target, const int64_t* labels, float* loss,
+                                void* grad_input, void* workspace, size_t workspace_bytes,
+                                fljsd_stream_t stream_) {
+  fljsd_status st = dist_common(rows, v, dtype, reduction, input, target, loss, grad_input,
+                                workspace, workspace_bytes);
+  if (st != FLJSD_OK) return st;
+  if (!(beta >= 0.f && beta <= 1.f)) return FLJSD_ERR_INVALID_ARG;
+  if (labels && !aligned16(labels)) return FLJSD_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* ws = static_cast<char*>(workspace);
+  float* loss_rows = reduction == FLJSD_RED_NONE ? loss : reinterpret_cast<float*>(ws);
+  int* n_valid = reinterpret_cast<int*>(ws + align_up((size_t)rows * sizeof(float)));
+  if (launch_count_valid(labels, rows, ignore_index, n_valid, stream) != cudaSuccess)
+    return FLJSD_ERR_CUDA;
+  DistArgs a{input, target, grad_input, rows, v, labels, ignore_index, n_valid, loss_rows,
+             nullptr, reduction, beta};
+  if (launch_jsd_logspace(dtype, a, stream) != cudaSuccess) return FLJSD_ERR_CUDA;
+  if (reduction != FLJSD_RED_NONE &&
+      launch_reduce_loss(loss_rows, rows, v, reduction, n_valid, loss, stream) != cudaSuccess)
+    return FLJSD_ERR_CUDA;
+  return FLJSD_OK;
+}
+
+fljsd_status fljsd_tvd(int64_t rows, int64_t v, int32_t dtype, int32_t reduction,
+                       int64_t ignore_index, const void* p, const void* q, const int64_t* labels,
+                       float* loss, void* grad_p, void* workspace, size_t workspace_bytes,
+                       fljsd_stream_t stream_) {
+  fljsd_status st = dist_common(rows, v, dtype, reduction, p, q, loss, grad_p, workspace,
+                                workspace_bytes);
+  if (st != FLJSD_OK) return st;
+  if (labels && !aligned16(labels)) return FLJSD_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* ws = static_cast<char*>(workspace);
+  float* loss_rows = reinterpret_cast<float*>(ws);
+  int* n_valid = reinterpret_cast<int*>(ws + align_up((size_t)rows * sizeof(float)));
+  if (launch_count_valid(labels, rows, ignore_index, n_valid, stream) != cudaSuccess)
+    return FLJSD_ERR_CUDA;
+  DistArgs a{p, q, grad_p, rows, v, labels, ignore_index, n_valid, loss_rows,
+             reduction == FLJSD_RED_NONE ? loss : nullptr, reduction, 0.f};
+  if (launch_tvd(dtype, a, stream) != cudaSuccess) return FLJSD_ERR_CUDA;
+  if (reduction != FLJSD_RED_NONE &&
+      launch_reduce_loss(loss_rows, rows, v, reduction, n_valid, loss, stream) != cudaSuccess)
+    return FLJSD_ERR_CUDA;
+  return FLJSD_OK;
+}
+
+fljsd_status fljsd_scale(int32_t dtype, void* x, int64_t n, const float* grad_output,
+                         fljsd_stream_t stream_) {
+  if ((dtype != FLJSD_F32 && dtype != FLJSD_BF16) || !x || !grad_output || n < 0)
+    return FLJSD_ERR_INVALID_ARG;
+  if (!aligned16(x) || ((uintptr_t)grad_output & 3u)) return FLJSD_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  return launch_scale(dtype, x, n, grad_output, stream) == cudaSuccess ? FLJSD_OK
+                                                                      : FLJSD_ERR_CUDA;
+}
+
 int64_t fljsd_launch_count(void) { return g_launches.load(); }
 void fljsd_launch_count_reset(void) { g_launches.store(0); }
 

@@ -53,6 +53,23 @@ cudaError_t launch_reduce_loss(const float* loss_rows, int64_t bt, int64_t v, in
                                const int* n_valid, float* loss, cudaStream_t st);
 cudaError_t launch_scale(int dtype, void* p, int64_t n, const float* g, cudaStream_t st);
 
+// Distances over given distributions (dist_rows.cu): log-space JSD and TVD.
+struct DistArgs {
+  const void* x;          // log-space JSD: input log Q; TVD: p   [rows x v]
+  const void* y;          // log-space JSD: target log P; TVD: q  [rows x v]
+  void* grad;             // d loss / d x, same dtype            [rows x v]
+  int64_t rows, v;
+  const int64_t* labels;  // [rows] or null
+  int64_t ignore_index;
+  const int* n_valid;
+  float* loss_rows;       // [rows]
+  float* loss_elem;       // TVD with reduction none: [rows x v] fp32, else null
+  int reduction;
+  float beta;
+};
+cudaError_t launch_jsd_logspace(int dtype, const DistArgs& a, cudaStream_t st);
+cudaError_t launch_tvd(int dtype, const DistArgs& a, cudaStream_t st);
+
 // ---------------------------------------------------------------------------
 // GEMMs. C[m, n] (+)= sum_k A(m, k) * B(n, k), fp32 accumulation, one rounding
 // to the output dtype. A(m, k) = A[m * sam + k * sak], B(n, k) = B[n * sbn + k * sbk].

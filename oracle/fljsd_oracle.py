@@ -303,28 +303,85 @@ def fljsd_rows_ref(x_s_rows, w_s, x_t_rows, w_t, *, beta: float, temperature: fl
 # ---------------------------------------------------------------------------
 # total variation distance (adjacent path; pins the batchmean reading)
 # ---------------------------------------------------------------------------
-def tvd_ref(p: np.ndarray, q: np.ndarray, reduction: str = "batchmean"):
+def _dist_weights(labels, rows: int, v: int, reduction: str, ignore_index: int):
+    """Row mask and per-row weight for the distances over given distributions
+    (same reductions as the fused loss; none -> weight 1)."""
+    w, valid, n = row_weights(labels, rows, v, "sum" if reduction == "none" else reduction,
+                              ignore_index)
+    return valid, n, w
+
+
+def tvd_ref(p: np.ndarray, q: np.ndarray, reduction: str = "batchmean", labels=None,
+            ignore_index: int = -100):
     """TVD loss 0.5*|p - q| summed over the vocabulary and its gradient in p.
 
     "Fix TVD gradient at p == q" (PR 1374), "Summary": the derivative of
     0.5*|p - q| is +0.5 where p > q, -0.5 where p < q, and exactly 0 at p == q
     (the three-way sign). Reductions follow the same readings as the JSD; the
     tie table of that page fixes batchmean as division by the number of rows.
-    Returns (loss, grad_p).
+    Rows whose label is ignore_index give loss 0 and gradient 0.
+    Returns (loss, grad_p); loss is per element [rows x V] for none.
     """
     p = np.asarray(p, dtype=np.float64)
     q = np.asarray(q, dtype=np.float64)
     rows, v = p.shape
-    per_elem = 0.5 * np.abs(p - q)
-    sign = np.where(p > q, 1.0, np.where(p < q, -1.0, 0.0))
-    if reduction == "none":
-        return per_elem, 0.5 * sign
-    if reduction == "sum":
-        scale = 1.0
-    elif reduction == "batchmean":
-        scale = 1.0 / rows
-    elif reduction == "mean":
-        scale = 1.0 / (rows * v)
-    else:
+    if reduction not in REDUCTIONS:
         raise ValueError(reduction)
-    return float(per_elem.sum() * scale), 0.5 * sign * scale
+    valid, n, w = _dist_weights(labels, rows, v, reduction, ignore_index)
+    per_elem = np.where(valid[:, None], 0.5 * np.abs(p - q), 0.0)
+    sign = np.where(p > q, 1.0, np.where(p < q, -1.0, 0.0))
+    grad = 0.5 * sign * w[:, None]
+    if reduction == "none":
+        return per_elem, grad
+    total = per_elem.sum()
+    if n == 0:
+        return 0.0, grad
+    scale = {"sum": 1.0, "batchmean": 1.0 / n, "mean": 1.0 / (n * v)}[reduction]
+    return float(total * scale), grad
+
+
+def jsd_logspace_ref(x: np.ndarray, y: np.ndarray, *, beta: float = 0.5,
+                     reduction: str = "batchmean", labels=None, ignore_index: int = -100):
+    """The generalized JSD on given log-probabilities and its gradient in X.
+
+    The public contract of Liger's _jsd_kernel ("[Perf] Fuse log-softmax into
+    fused_linear_jsd kernel", PR 1352, Open questions 3): the inputs are
+    log-probabilities already, X = log Q (input, student) and Y = log P
+    (target, teacher). Per element, with P = e^Y, Q = e^X and
+    M = beta P + (1 - beta) Q: beta = 0 gives P (Y - X), beta = 1 gives
+    Q (X - Y), otherwise beta P (Y - log M) + (1 - beta) Q (X - log M). The
+    gradient is taken element by element with X as the free variable (the
+    inputs are not renormalised): -P, Q (X - Y + 1), and (1 - beta) Q (X - log M).
+    The tie rule of PR 1374 gives a zero loss term at X == Y, and a zero
+    gradient where the calculus does (the generalized branch).
+    Returns (loss, grad_x); loss is per row [rows] for none.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    rows, v = x.shape
+    if not (0.0 <= beta <= 1.0):
+        raise ValueError("beta must be in [0, 1]")
+    valid, n, w = _dist_weights(labels, rows, v, reduction, ignore_index)
+    P, Q = np.exp(y), np.exp(x)
+    tie = x == y
+    if beta == 0.0:
+        ell = np.where(tie, 0.0, P * (y - x))
+        g = -P
+    elif beta == 1.0:
+        ell = np.where(tie, 0.0, Q * (x - y))
+        g = Q * (x - y + 1.0)
+    else:
+        M = beta * P + (1.0 - beta) * Q
+        zero = tie | (M == 0.0)
+        logM = np.log(np.where(M == 0.0, 1.0, M))
+        ell = np.where(zero, 0.0, beta * P * (y - logM) + (1.0 - beta) * Q * (x - logM))
+        g = np.where(zero, 0.0, (1.0 - beta) * Q * (x - logM))
+    rows_loss = np.where(valid, ell.sum(axis=1), 0.0)
+    grad = g * w[:, None]
+    grad[~valid] = 0.0
+    if reduction == "none":
+        return rows_loss, grad
+    if n == 0:
+        return 0.0, grad
+    scale = {"sum": 1.0, "batchmean": 1.0 / n, "mean": 1.0 / (n * v)}[reduction]
+    return float(rows_loss.sum() * scale), grad

@@ -401,3 +401,88 @@ def test_t2_scaling_reaches_the_high_temperature_limit():
                                 t2_scale=True)
     assert loss2 == pytest.approx(4.0 * loss1, rel=1e-14)
     np.testing.assert_allclose(gi2, 4.0 * gi1, rtol=1e-14)
+
+
+
+# ---------------------------------------------------------------------------
+# distances over given distributions
+# ---------------------------------------------------------------------------
+def _logprobs(seed, rows=5, v=23, scale=2.0):
+    r = _rng(seed)
+    a = r.standard_normal((rows, v)) * scale
+    b = r.standard_normal((rows, v)) * scale
+    lp = lambda z: z - np.log(np.exp(z - z.max(1, keepdims=True)).sum(1, keepdims=True)) \
+        - z.max(1, keepdims=True)  # noqa: E731
+    return lp(a), lp(b)
+
+
+def test_logspace_endpoints_are_library_kl_with_autograd_gradients():
+    from oracle import jsd_logspace_ref
+
+    X, Y = _logprobs(30)
+    for beta, inp, tgt in ((0.0, X, Y), (1.0, Y, X)):
+        loss, grad = jsd_logspace_ref(X, Y, beta=beta, reduction="sum")
+        xt = torch.tensor(X, requires_grad=True)
+        yt = torch.tensor(Y)
+        a, b = (xt, yt) if beta == 0.0 else (yt, xt)
+        ref = torch.nn.functional.kl_div(a, b, log_target=True, reduction="sum")
+        ref.backward()
+        assert loss == pytest.approx(ref.item(), rel=1e-12)
+        np.testing.assert_allclose(grad, xt.grad.numpy(), rtol=1e-12, atol=1e-15)
+
+
+@pytest.mark.parametrize("beta", [0.1, 0.5, 0.8])
+def test_logspace_generalized_matches_entropy_form_and_finite_differences(beta):
+    from oracle import jsd_logspace_ref
+
+    X, Y = _logprobs(31)
+    rows, _ = jsd_logspace_ref(X, Y, beta=beta, reduction="none")
+    for r in range(X.shape[0]):
+        q = [math.exp(t) for t in X[r]]
+        p = [math.exp(t) for t in Y[r]]
+        m = [beta * a + (1 - beta) * b for a, b in zip(p, q)]
+        ent = lambda d: -sum(t * math.log(t) for t in d)  # noqa: E731
+        assert rows[r] == pytest.approx(ent(m) - beta * ent(p) - (1 - beta) * ent(q), rel=1e-10)
+    # gradient in X as free variables
+    _, grad = jsd_logspace_ref(X, Y, beta=beta, reduction="batchmean")
+    eps = 1e-6
+    num = np.zeros_like(X)
+    for i in range(X.shape[0]):
+        for j in range(X.shape[1]):
+            a, b = X.copy(), X.copy()
+            a[i, j] += eps; b[i, j] -= eps
+            num[i, j] = (jsd_logspace_ref(a, Y, beta=beta)[0] - jsd_logspace_ref(b, Y, beta=beta)[0]) / (2 * eps)
+    assert np.linalg.norm(num - grad) <= 1e-6 * np.linalg.norm(grad)
+
+
+def test_logspace_ties_ignored_rows_and_reductions():
+    from oracle import jsd_logspace_ref
+
+    X, Y = _logprobs(32, rows=6)
+    Y[2] = X[2]  # a fully tied row
+    labels = np.array([0, -100, 3, 4, 5, 6])
+    rows, g = jsd_logspace_ref(X, Y, beta=0.5, reduction="none", labels=labels)
+    assert rows[2] == 0.0 and np.all(g[2] == 0.0)
+    assert rows[1] == 0.0 and np.all(g[1] == 0.0)
+    s, _ = jsd_logspace_ref(X, Y, beta=0.5, reduction="sum", labels=labels)
+    b, _ = jsd_logspace_ref(X, Y, beta=0.5, reduction="batchmean", labels=labels)
+    m, _ = jsd_logspace_ref(X, Y, beta=0.5, reduction="mean", labels=labels)
+    assert s == pytest.approx(rows.sum()) and b == pytest.approx(s / 5)
+    assert m == pytest.approx(s / (5 * X.shape[1]))
+
+
+def test_tvd_matches_library_l1_and_autograd_off_ties():
+    r = _rng(33)
+    p = r.dirichlet(np.ones(40), size=6)
+    q = r.dirichlet(np.ones(40), size=6)
+    loss, grad = tvd_ref(p, q, reduction="sum")
+    pt = torch.tensor(p, requires_grad=True)
+    ref = 0.5 * torch.nn.functional.l1_loss(pt, torch.tensor(q), reduction="sum")
+    ref.backward()
+    assert loss == pytest.approx(ref.item(), rel=1e-13)
+    np.testing.assert_allclose(grad, pt.grad.numpy(), rtol=0, atol=0)
+    labels = np.array([1, -100, 2, 3, -100, 5])
+    lb, gb = tvd_ref(p, q, reduction="batchmean", labels=labels)
+    valid = labels != -100
+    assert lb == pytest.approx(0.5 * np.abs(p - q)[valid].sum() / 4)
+    assert np.all(gb[~valid] == 0.0)
