@@ -198,7 +198,12 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--ref-rows", type=int, default=16,
                     help="rows per step of the reference (oracle) arm")
+    ap.add_argument("--path", default="fljsd", choices=["fljsd", "jsd_logspace", "tvd"],
+                    help="fljsd: the fused-linear JSD (the headline); the others measure the "
+                         "distance kernels over given distributions")
     args = ap.parse_args()
+    if args.path != "fljsd":
+        return run_dist_bench(args)
 
     import torch
 
@@ -385,6 +390,68 @@ def run_e2e(torch, run, w, x_s, w_s, x_t, w_t, labels, steps, dist, world, dev):
             "d2h_bytes_per_step": host_loss.numel() * 4,
             "what": "pinned-host X_s, X_t, labels -> device; fljsd_forward + fljsd_backward; "
                     "loss -> host; wall clock per step, stream synchronised every step"}
+
+
+def run_dist_bench(args):
+    """Time one distance kernel (log-space JSD or TVD) on a [rows x V] bf16
+    problem larger than L2; HBM roofline on 3 * rows * V * 2 bytes (read two
+    tensors, write the gradient)."""
+    import torch
+
+    import jsd_inputs
+    from lm_head_jsd_gb300 import _lib
+
+    # TVD: the shape the tie-fix page timed (4096 x 32000 bf16); log-space JSD:
+    # the fused path's BT x V.
+    rows, v = (4096, 32000) if args.path == "tvd" else (8192, 128256)
+    dev = torch.device("cuda", 0)
+    a, b, _ = jsd_inputs.make_distributions(rows, v, "bf16", 100, logspace=args.path != "tvd",
+                                            device=str(dev))
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    grad = torch.empty_like(a)
+    ws = torch.empty(_lib.fljsd_rows_workspace_bytes(rows), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        if args.path == "tvd":
+            _lib.fljsd_tvd(rows, v, "bf16", "batchmean", -100, a, b, None, loss, grad, ws,
+                           stream=stream)
+        else:
+            _lib.fljsd_jsd_logspace(rows, v, "bf16", 0.5, "batchmean", -100, a, b, None, loss,
+                                    grad, ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize(dev)
+    _lib.fljsd_trace_enable(4 * args.steps + 8)
+    _lib.fljsd_trace_reset()
+    n0 = _lib.fljsd_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        call()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    k_ms, k_n = _lib.fljsd_trace_read("jsd_rows")
+    _lib.fljsd_trace_enable(0)
+    peaks = _peaks()
+    bytes_ = 3 * rows * v * 2
+    kern_ms = k_ms / max(k_n, 1)
+    gbs = bytes_ / (kern_ms / 1e3) / 1e9
+    name = "TVD fwd+bwd" if args.path == "tvd" else "log-space JSD fwd+bwd"
+    print(json.dumps({
+        "metric": f"{name} rows/s at ({rows}, {v}) bf16", "value": round(rows / (ms / 1e3), 1),
+        "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.path}: rows={rows} V={v} bf16 batchmean",
+                   "l2": "inputs larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                     "algorithmic_bytes": "3*rows*V*2 per call"},
+        "gpu_launches": _lib.fljsd_launch_count() - n0}), flush=True)
+    return 0
 
 
 def run_reference(args, w, world):
