@@ -264,6 +264,42 @@ fljsd_status fljsd_tvd(int64_t rows, int64_t v, int32_t dtype, int32_t reduction
 fljsd_status fljsd_scale(int32_t dtype, void* x, int64_t n, const float* grad_output,
                          fljsd_stream_t stream);
 
+/*
+ * Fused linear cross-entropy (FLCE): loss = CE(x . w^T, labels) and its
+ * gradients in x and w, on the same GEMMs, chunk planner and grad_weight
+ * contract as fljsd_forward ("perf(flce): write the weight-gradient product
+ * directly into grad_weight", PR 1429: first chunk overwrites, later chunks add
+ * in fp32 and round once, or accumulate in fp32 with FLJSD_FLAG_ACCUM_FP32).
+ * Per row with label y and logits z (c = softcap * tanh(z / softcap) when
+ * softcap > 0, else c = z), lse = log sum_j e^{c_j}:
+ *   L = lse - (1 - eps) c_y - (eps / V) sum_j c_j + lse_square_scale * lse^2
+ * (eps = label_smoothing). Reductions: none -> [bt] per-row losses; sum;
+ * mean and batchmean -> divided by the number of rows whose label is not
+ * ignore_index. Labels are required (int64 [bt], device); a label outside
+ * [0, v) that is not ignore_index makes its row contribute 0 and sets the
+ * workspace status word to FLJSD_ERR_INVALID_ARG (fljsd_workspace_status).
+ * x [bt x h], w [v x h], grad_input [bt x h], grad_weight [v x h] in dtype.
+ * Gradients are for an upstream gradient of 1 (fljsd_scale applies another).
+ */
+typedef struct {
+  int64_t bt, h, v;
+  int32_t dtype;          /* fljsd_dtype */
+  int32_t reduction;      /* fljsd_reduction */
+  int64_t ignore_index;
+  int64_t chunk_rows;     /* 0 lets fljsd_ce_plan choose */
+  float label_smoothing;  /* in [0, 1] */
+  float lse_square_scale; /* z-loss coefficient, >= 0 */
+  float softcap;          /* 0 disables the tanh cap */
+  int32_t flags;          /* FLJSD_FLAG_ACCUM_FP32 or 0 */
+} fljsd_ce_problem;
+
+fljsd_status fljsd_ce_plan(const fljsd_ce_problem* problem, size_t free_hbm_bytes,
+                           fljsd_plan_t* out);
+fljsd_status fljsd_ce_forward(const fljsd_ce_problem* problem, const fljsd_plan_t* plan,
+                              const void* x, const void* w, const int64_t* labels, float* loss,
+                              void* grad_input, void* grad_weight, void* workspace,
+                              size_t workspace_bytes, fljsd_stream_t stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 const char* fljsd_status_string(fljsd_status status);
 

@@ -169,3 +169,20 @@ def make_distributions(rows: int, v: int, dtype: str, seed: int, *, logspace: bo
     if labels is not None:
         labels = labels.to(device)
     return a.contiguous(), b.contiguous(), labels
+
+
+def make_ce_inputs(bt: int, h: int, v: int, dtype: str, seed: int, *, ignore_frac: float = 0.0,
+                   device: str = "cpu"):
+    """Hidden states x [BT x H] ~ N(0, 1), lm_head weight w [V x H] ~ N(0, 1/H)
+    (float32, cast to the dtype) and int64 labels uniform in [0, V) with
+    floor(frac*BT) rows set to -100: the cross-entropy path's inputs."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    x = _randn((bt, h), 1.0, g, device)
+    w = _randn((v, h), 1.0 / math.sqrt(h), g, device)
+    dt = torch.float32 if dtype == "fp32" else torch.bfloat16
+    lg = torch.Generator().manual_seed(seed)
+    labels = torch.randint(0, v, (bt,), generator=lg, dtype=torch.int64)
+    n_ign = int(math.floor(ignore_frac * bt))
+    if n_ign:
+        labels[torch.randperm(bt, generator=lg)[:n_ign]] = IGNORE_INDEX
+    return x.to(dt), w.to(dt), labels.to(device)

@@ -7,6 +7,9 @@ points by name, ``api`` adds torch allocation and an autograd Function.
 from ._lib import (  # noqa: F401
     FljsdError,
     fljsd_backward,
+    fljsd_ce_forward,
+    fljsd_ce_plan,
+    make_ce_problem,
     fljsd_forward,
     fljsd_forward_noalloc,
     fljsd_gemm_bf16,
@@ -24,6 +27,13 @@ from ._lib import (  # noqa: F401
     fljsd_workspace_status,
     make_problem,
 )
-from .api import FusedLinearJSD, fused_linear_jsd, jsd_logspace, tvd  # noqa: F401
+from .api import (  # noqa: F401
+    FusedLinearCrossEntropy,
+    FusedLinearJSD,
+    fused_linear_cross_entropy,
+    fused_linear_jsd,
+    jsd_logspace,
+    tvd,
+)
 
 LIB_PATH = _lib.LIB_PATH

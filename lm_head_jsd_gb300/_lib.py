@@ -37,6 +37,14 @@ class fljsd_problem(ctypes.Structure):
                 ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+class fljsd_ce_problem(ctypes.Structure):
+    _fields_ = [("bt", ctypes.c_int64), ("h", ctypes.c_int64), ("v", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("reduction", ctypes.c_int32),
+                ("ignore_index", ctypes.c_int64), ("chunk_rows", ctypes.c_int64),
+                ("label_smoothing", ctypes.c_float), ("lse_square_scale", ctypes.c_float),
+                ("softcap", ctypes.c_float), ("flags", ctypes.c_int32)]
+
+
 FLJSD_FLAG_T2 = 1
 FLJSD_FLAG_ACCUM_FP32 = 2
 
@@ -83,6 +91,13 @@ def _load():
     lib.fljsd_tvd.restype = ctypes.c_int
     lib.fljsd_scale.argtypes = [ctypes.c_int32, P, ctypes.c_int64, P, P]
     lib.fljsd_scale.restype = ctypes.c_int
+    lib.fljsd_ce_plan.argtypes = [ctypes.POINTER(fljsd_ce_problem), ctypes.c_size_t,
+                                  ctypes.POINTER(fljsd_plan_t)]
+    lib.fljsd_ce_plan.restype = ctypes.c_int
+    lib.fljsd_ce_forward.argtypes = [ctypes.POINTER(fljsd_ce_problem),
+                                     ctypes.POINTER(fljsd_plan_t), P, P, P, P, P, P, P,
+                                     ctypes.c_size_t, P]
+    lib.fljsd_ce_forward.restype = ctypes.c_int
     lib.fljsd_status_string.argtypes = [ctypes.c_int]
     lib.fljsd_status_string.restype = ctypes.c_char_p
     lib.fljsd_launch_count.argtypes = []
@@ -236,6 +251,34 @@ def fljsd_scale(dtype, x, n, grad_output, stream=None, check=True) -> int:
     st = lib.fljsd_scale(_dt(dtype), _ptr(x), n, _ptr(grad_output), _stream(stream))
     if check and st != FLJSD_OK:
         raise FljsdError(st, "fljsd_scale")
+    return st
+
+
+def make_ce_problem(bt, h, v, dtype="bf16", reduction="mean", ignore_index=-100, chunk_rows=0,
+                    label_smoothing=0.0, lse_square_scale=0.0, softcap=0.0,
+                    accum_fp32=False) -> fljsd_ce_problem:
+    return fljsd_ce_problem(bt, h, v, _dt(dtype), _red(reduction), ignore_index, chunk_rows,
+                            label_smoothing, lse_square_scale, softcap,
+                            FLJSD_FLAG_ACCUM_FP32 if accum_fp32 else 0)
+
+
+def fljsd_ce_plan(problem, free_hbm_bytes: int = 0) -> fljsd_plan_t:
+    plan = fljsd_plan_t()
+    st = lib.fljsd_ce_plan(ctypes.byref(problem), free_hbm_bytes, ctypes.byref(plan))
+    if st != FLJSD_OK:
+        raise FljsdError(st, "fljsd_ce_plan")
+    return plan
+
+
+def fljsd_ce_forward(problem, plan, x, w, labels, loss, grad_input, grad_weight, workspace,
+                     workspace_bytes=None, stream=None, check=True) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = lib.fljsd_ce_forward(ctypes.byref(problem), ctypes.byref(plan), _ptr(x), _ptr(w),
+                              _ptr(labels), _ptr(loss), _ptr(grad_input), _ptr(grad_weight),
+                              _ptr(workspace), workspace_bytes, _stream(stream))
+    if check and st != FLJSD_OK:
+        raise FljsdError(st, "fljsd_ce_forward")
     return st
 
 

@@ -181,4 +181,80 @@ def tvd(p, q, labels=None, *, reduction="batchmean", ignore_index=-100):
     return _DistFunction.apply("tvd", p, q, labels, reduction, int(ignore_index), 0.0)
 
 
-__all__ = ["FusedLinearJSD", "fused_linear_jsd", "jsd_logspace", "tvd", "_lib"]
+class FusedLinearCrossEntropy:
+    """Plans one FLCE problem shape and keeps its workspace (see fljsd_ce_forward)."""
+
+    def __init__(self, bt, h, v, dtype=torch.bfloat16, *, reduction="mean", ignore_index=-100,
+                 label_smoothing=0.0, lse_square_scale=0.0, softcap=0.0, chunk_rows=0,
+                 accum_fp32=False, device="cuda", free_hbm_bytes=None):
+        self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        self.dtype = dtype
+        self.reduction = reduction
+        self.problem = _lib.make_ce_problem(bt, h, v, _DT[dtype], reduction, ignore_index,
+                                            chunk_rows, label_smoothing, lse_square_scale,
+                                            softcap, accum_fp32)
+        if free_hbm_bytes is None:
+            free_hbm_bytes = torch.cuda.mem_get_info(self.device)[0]
+        self.plan = _lib.fljsd_ce_plan(self.problem, int(free_hbm_bytes))
+        self.workspace = torch.empty(self.plan.workspace_bytes, dtype=torch.uint8,
+                                     device=self.device)
+
+    def alloc_outputs(self):
+        p = self.problem
+        loss = torch.empty(p.bt if self.reduction == "none" else 1, dtype=torch.float32,
+                           device=self.device)
+        gi = torch.empty(p.bt, p.h, dtype=self.dtype, device=self.device)
+        gw = torch.empty(p.v, p.h, dtype=self.dtype, device=self.device)
+        return loss, gi, gw
+
+    def forward(self, x, w, labels, out=None, stream=None):
+        p = self.problem
+        _check("x", x, self.dtype, self.device, (p.bt, p.h))
+        _check("w", w, self.dtype, self.device, (p.v, p.h))
+        _check("labels", labels, torch.int64, self.device, (p.bt,))
+        loss, gi, gw = self.alloc_outputs() if out is None else out
+        _lib.fljsd_ce_forward(p, self.plan, x, w, labels, loss, gi, gw, self.workspace,
+                              stream=stream)
+        return loss, gi, gw
+
+
+class _FLCEFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, w, labels, reduction, ignore_index, label_smoothing, lse_square_scale,
+                softcap, chunk_rows):
+        run = FusedLinearCrossEntropy(x.shape[0], x.shape[1], w.shape[0], x.dtype,
+                                      reduction=reduction, ignore_index=ignore_index,
+                                      label_smoothing=label_smoothing,
+                                      lse_square_scale=lse_square_scale, softcap=softcap,
+                                      chunk_rows=chunk_rows, device=x.device)
+        loss, gi, gw = run.forward(x.detach().contiguous(), w.detach().contiguous(),
+                                   labels.contiguous())
+        if reduction == "none":
+            raise NotImplementedError("use reduction sum or mean through autograd")
+        ctx.save_for_backward(gi, gw)
+        ctx.dtype = x.dtype
+        return loss.reshape(())
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        gi, gw = ctx.saved_tensors
+        g = grad_out.detach().to(torch.float32).reshape(1).contiguous()
+        _lib.fljsd_scale(_DT[ctx.dtype], gi, gi.numel(), g)
+        _lib.fljsd_scale(_DT[ctx.dtype], gw, gw.numel(), g)
+        return gi, gw, None, None, None, None, None, None, None
+
+
+def fused_linear_cross_entropy(x, w, labels, *, reduction="mean", ignore_index=-100,
+                               label_smoothing=0.0, lse_square_scale=0.0, softcap=0.0,
+                               chunk_rows=0):
+    """Cross-entropy of the logits x.w^T against int64 labels, differentiable in
+    x and w (reduction sum or mean through autograd)."""
+    return _FLCEFunction.apply(x, w, labels, reduction, int(ignore_index),
+                               float(label_smoothing), float(lse_square_scale), float(softcap),
+                               int(chunk_rows))
+
+
+__all__ = ["FusedLinearJSD", "fused_linear_jsd", "jsd_logspace", "tvd",
+           "FusedLinearCrossEntropy", "fused_linear_cross_entropy", "_lib"]

@@ -10,6 +10,7 @@ from .fljsd_oracle import (  # noqa: F401
     fljsd_from_logits,
     fljsd_ref,
     fljsd_rows_ref,
+    flce_ref,
     jsd_logspace_ref,
     jsd_rows,
     log_softmax_rows,

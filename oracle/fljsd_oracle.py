@@ -385,3 +385,59 @@ def jsd_logspace_ref(x: np.ndarray, y: np.ndarray, *, beta: float = 0.5,
         return 0.0, grad
     scale = {"sum": 1.0, "batchmean": 1.0 / n, "mean": 1.0 / (n * v)}[reduction]
     return float(rows_loss.sum() * scale), grad
+
+
+# ---------------------------------------------------------------------------
+# fused linear cross-entropy (the FLCE path)
+# ---------------------------------------------------------------------------
+def flce_ref(x, w, labels, *, reduction: str = "mean", ignore_index: int = -100,
+             label_smoothing: float = 0.0, lse_square_scale: float = 0.0, softcap: float = 0.0,
+             block_rows: int = 256):
+    """Cross-entropy of the logits x . w^T and its gradients in x and w.
+
+    "perf(flce): write the weight-gradient product directly into grad_weight"
+    (PR 1429): grad_weight is the sum over row chunks of dlogits^T . x; the
+    page's tests exercise label smoothing, z-loss, softcap and reduction none.
+    Per row with label y: c = softcap * tanh(z / softcap) (or z), lse =
+    logsumexp(c), L = lse - (1 - eps) c_y - eps * mean_j(c_j) + lambda lse^2.
+    Reductions: none -> per row; sum; mean (and batchmean) -> divided by the
+    rows whose label is not ignore_index. Returns (loss, grad_input, grad_weight).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    labels = np.asarray(labels).reshape(-1)
+    bt, h = x.shape
+    v = w.shape[0]
+    valid = labels != ignore_index
+    n = int(valid.sum())
+    if reduction == "none" or reduction == "sum":
+        scale = 1.0
+    else:
+        scale = 1.0 / n if n > 0 else 0.0
+    eps, lam = label_smoothing, lse_square_scale
+    loss_rows = np.zeros(bt)
+    gi = np.zeros((bt, h))
+    gw = np.zeros((v, h))
+    for r0 in range(0, bt, block_rows):
+        r1 = min(bt, r0 + block_rows)
+        z = logits(x[r0:r1], w)
+        c = softcap * np.tanh(z / softcap) if softcap > 0.0 else z
+        m = c.max(axis=1, keepdims=True)
+        lse = (m + np.log(np.exp(c - m).sum(axis=1, keepdims=True)))[:, 0]
+        p = np.exp(c - lse[:, None])
+        vb = valid[r0:r1]
+        y = np.where(vb, labels[r0:r1], 0)
+        cy = c[np.arange(r1 - r0), y]
+        L = lse - (1.0 - eps) * cy - eps * c.mean(axis=1) + lam * lse ** 2
+        loss_rows[r0:r1] = np.where(vb, L, 0.0)
+        dc = p * (1.0 + 2.0 * lam * lse)[:, None] - eps / v
+        dc[np.arange(r1 - r0), y] -= (1.0 - eps)
+        if softcap > 0.0:
+            dc = dc * (1.0 - (c / softcap) ** 2)
+        dc[~vb] = 0.0
+        dz = dc * scale
+        gi[r0:r1] = dz @ w
+        gw += dz.T @ x[r0:r1]
+    if reduction == "none":
+        return loss_rows, gi, gw
+    return float(loss_rows.sum() * scale), gi, gw

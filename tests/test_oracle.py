@@ -486,3 +486,51 @@ def test_tvd_matches_library_l1_and_autograd_off_ties():
     valid = labels != -100
     assert lb == pytest.approx(0.5 * np.abs(p - q)[valid].sum() / 4)
     assert np.all(gb[~valid] == 0.0)
+
+
+# ---------------------------------------------------------------------------
+# fused linear cross-entropy
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("eps", [0.0, 0.1])
+@pytest.mark.parametrize("red", ["mean", "sum", "none"])
+def test_flce_loss_is_library_cross_entropy(eps, red):
+    from oracle import flce_ref
+
+    x_s, w_s, _, _ = _problem(40, bt=9, h=6, v=30)
+    labels = np.array([3, -100, 0, 29, 7, 7, -100, 1, 12])
+    loss, gi, gw = flce_ref(x_s, w_s, labels, reduction=red, label_smoothing=eps)
+    xt = torch.tensor(x_s, requires_grad=True)
+    wt = torch.tensor(w_s, requires_grad=True)
+    ref = torch.nn.functional.cross_entropy(xt @ wt.T, torch.tensor(labels), ignore_index=-100,
+                                            label_smoothing=eps, reduction=red)
+    if red == "none":
+        np.testing.assert_allclose(loss, ref.detach().numpy(), rtol=1e-12, atol=1e-14)
+        ref = ref.sum()
+    else:
+        assert loss == pytest.approx(ref.item(), rel=1e-12)
+    ref.backward()
+    np.testing.assert_allclose(gi, xt.grad.numpy(), rtol=1e-10, atol=1e-14)
+    np.testing.assert_allclose(gw, wt.grad.numpy(), rtol=1e-10, atol=1e-14)
+
+
+def test_flce_softcap_and_z_loss_gradients_match_autograd():
+    from oracle import flce_ref
+
+    x_s, w_s, _, _ = _problem(41, bt=7, h=5, v=20, scale=3.0)
+    labels = np.array([0, 5, -100, 19, 3, 3, 8])
+    cap, lam, eps = 2.5, 1e-3, 0.05
+    loss, gi, gw = flce_ref(x_s, w_s, labels, reduction="mean", label_smoothing=eps,
+                            lse_square_scale=lam, softcap=cap)
+    xt = torch.tensor(x_s, requires_grad=True)
+    wt = torch.tensor(w_s, requires_grad=True)
+    c = cap * torch.tanh((xt @ wt.T) / cap)
+    lab = torch.tensor(labels)
+    valid = lab != -100
+    lse = torch.logsumexp(c, dim=1)
+    ce = torch.nn.functional.cross_entropy(c, lab, ignore_index=-100, label_smoothing=eps,
+                                           reduction="sum")
+    ref = (ce + lam * (lse[valid] ** 2).sum()) / valid.sum()
+    ref.backward()
+    assert loss == pytest.approx(ref.item(), rel=1e-12)
+    np.testing.assert_allclose(gi, xt.grad.numpy(), rtol=1e-10, atol=1e-14)
+    np.testing.assert_allclose(gw, wt.grad.numpy(), rtol=1e-10, atol=1e-14)
