@@ -198,10 +198,12 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--ref-rows", type=int, default=16,
                     help="rows per step of the reference (oracle) arm")
-    ap.add_argument("--path", default="fljsd", choices=["fljsd", "jsd_logspace", "tvd"],
+    ap.add_argument("--path", default="fljsd", choices=["fljsd", "jsd_logspace", "tvd", "flce"],
                     help="fljsd: the fused-linear JSD (the headline); the others measure the "
                          "distance kernels over given distributions")
     args = ap.parse_args()
+    if args.path == "flce":
+        return run_flce_bench(args)
     if args.path != "fljsd":
         return run_dist_bench(args)
 
@@ -451,6 +453,70 @@ def run_dist_bench(args):
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
                      "algorithmic_bytes": "3*rows*V*2 per call"},
         "gpu_launches": _lib.fljsd_launch_count() - n0}), flush=True)
+    return 0
+
+
+def run_flce_bench(args):
+    """Fused linear cross-entropy fwd+bwd at BT=8192, H=4096, V=128256 bf16,
+    reduction mean -- the shape of the grad_weight page's FLCE table (its H100
+    figure, 37.34 ms, is context on another machine). Tensor-core roofline on
+    6 * BT * V * H FLOPs."""
+    import torch
+
+    import jsd_inputs
+    import lm_head_jsd_gb300 as fl
+    from lm_head_jsd_gb300 import FusedLinearCrossEntropy
+
+    bt, h, v = 8192, 4096, 128256
+    dev = torch.device("cuda", 0)
+    x, w, labels = jsd_inputs.make_ce_inputs(bt, h, v, "bf16", 200, device=str(dev))
+    run = FusedLinearCrossEntropy(bt, h, v, torch.bfloat16, chunk_rows=args.chunk_rows,
+                                  device=dev)
+    loss, gi, gw = run.alloc_outputs()
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        run.forward(x, w, labels, out=(loss, gi, gw), stream=stream)
+        fl.fljsd_scale("bf16", gi, gi.numel(), one, stream=stream)
+        fl.fljsd_scale("bf16", gw, gw.numel(), one, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    fl.fljsd_trace_enable(args.steps * (4 * run.plan.num_chunks + 4) + 16)
+    fl.fljsd_trace_reset()
+    n0 = fl.fljsd_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    kinds = {k: fl.fljsd_trace_read(k) for k in
+             ("gemm_logits", "jsd_rows", "gemm_grad_input", "gemm_grad_weight", "small")}
+    fl.fljsd_trace_enable(0)
+    peaks = _peaks()
+    flop = 6.0 * bt * v * h
+    g_ms = sum(kinds[k][0] for k in ("gemm_logits", "gemm_grad_input", "gemm_grad_weight"))
+    g_n = sum(kinds[k][1] for k in ("gemm_logits", "gemm_grad_input", "gemm_grad_weight"))
+    achieved = (flop / 3) / (g_ms / g_n / 1e3) / 1e12 if g_n else float("nan")
+    peak = peaks["bf16_tflops_sustained"]
+    print(json.dumps({
+        "metric": "fused-linear cross-entropy fwd+bwd tokens/s at H=4096,V=128256 bf16",
+        "value": round(bt / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"flce: BT={bt} H={h} V={v} bf16 mean",
+                   "chunk_rows": int(run.plan.chunk_rows)},
+        "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (3 launches per chunk)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None},
+        "roofline_step": {"flop": flop, "frac": round(flop / (peak * 1e12) * 1e3 / ms, 4)},
+        "kernel_ms_per_step": {k: round(t / args.steps, 4) for k, (t, _) in kinds.items()},
+        "gpu_launches": fl.fljsd_launch_count() - n0}), flush=True)
     return 0
 
 
