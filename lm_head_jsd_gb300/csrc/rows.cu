@@ -86,8 +86,24 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
   return r;
 }
 
+// Generalized-branch terms of one bf16 element for the lean path: X2, Y2 from
+// one fma each, P, Q, and the log ratios X - log M, Y - log M (both exactly 0
+// at a tie), in log2 units.
+__device__ __forceinline__ void lean_terms(float zs, float zt, float c, float oa, float ob,
+                                           float beta, float omb, float& Q, float& P,
+                                           float& xm, float& ym) {
+  const float X2 = __fmaf_rn(zs, c, -oa);
+  const float Y2 = __fmaf_rn(zt, c, -ob);
+  Q = ex2(X2);
+  P = ex2(Y2);
+  const float lM = lg2(fmaxf(fmaf(omb, Q, beta * P), 1.17549435e-38f));
+  const bool tie = X2 == Y2;
+  xm = tie ? 0.f : X2 - lM;
+  ym = tie ? 0.f : Y2 - lM;
+}
+
 template <typename T, int BRANCH>
-__global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
+__global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
   using V = Vec<T>;
   constexpr bool PREC = sizeof(T) == 4;
   constexpr int N = V::N;
@@ -162,6 +178,60 @@ __global__ void __launch_bounds__(kRowThreads) k_jsd_rows(JsdRowArgs a) {
     const float lda = single ? 0.f : plog2<PREC>(ra.d);
     const float ldb = single ? 0.f : plog2<PREC>(rb.d);
     const float cz = single ? 0.f : c;
+
+    // Lean path for the generalized branch on bf16 logits: the two row offsets
+    // fold into one fma per element (exact to 2^-18 in log2 units while the
+    // row maxima are below 64, a constant per-row shift that the loss does not
+    // feel at first order), and the per-element products accumulate with fmas:
+    // S = (1-beta) sum Q xm, L = beta sum P ym + S.
+    if (BRANCH == 2 && !PREC && fabsf(ma_) < 64.f && fabsf(mb_) < 64.f) {
+      const float oa = ma_ + lda, ob = mb_ + ldb;
+      float accq = 0.f, accp = 0.f;
+      for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+        float xs[N], xt[N];
+        V::load(zs + i * N, xs);
+        V::load(zt + i * N, xt);
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          float Q, P, xm, ym;
+          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          accq = fmaf(Q, xm, accq);
+          accp = fmaf(P, ym, accp);
+        }
+      }
+      for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
+        float Q, P, xm, ym;
+        lean_terms(V::one(zs + j), V::one(zt + j), cz, oa, ob, beta, omb, Q, P, xm, ym);
+        accq = fmaf(Q, xm, accq);
+        accp = fmaf(P, ym, accp);
+      }
+      const float2 tot = block_sum2(make_float2(accq, accp), sh_s);
+      const float S2 = omb * tot.x;
+      const float L2 = fmaf(beta, tot.y, S2);
+      if (threadIdx.x == 0) a.loss_rows[grow] = 0.6931471805599453f * L2 * a.loss_scale;
+      // dz = ln2 * scale * Q * ((1-beta) xm - S)
+      const float k0 = 0.6931471805599453f * w * a.inv_temperature * a.loss_scale;
+      const float k1 = k0 * omb, k2 = k0 * S2;
+      for (int64_t i = nvec - 1 - threadIdx.x; i >= 0; i -= blockDim.x) {
+        float xs[N], xt[N];
+        V::load(zs + i * N, xs);
+        V::load(zt + i * N, xt);
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          float Q, P, xm, ym;
+          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          xs[k] = Q * fmaf(k1, xm, -k2);
+        }
+        V::store(zs + i * N, xs);
+      }
+      for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
+        float Q, P, xm, ym;
+        lean_terms(V::one(zs + j), V::one(zt + j), cz, oa, ob, beta, omb, Q, P, xm, ym);
+        V::put(zs + j, Q * fmaf(k1, xm, -k2));
+      }
+      __syncthreads();
+      continue;
+    }
 
     // ---- pass 2: loss and dX_sum ----
     float2 acc = make_float2(0.f, 0.f);
