@@ -146,6 +146,25 @@ def _gpu_index(torch, dev) -> str:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank host logic (replicas: no collective on the data path)
+# ---------------------------------------------------------------------------
+def reduce_max(value: float, dist, device) -> float:
+    """Largest `value` over all ranks (the slowest replica's time)."""
+    if dist is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(world: int, bt: int, ms_per_step: float) -> float:
+    """Tokens all replicas processed per second: each rank runs the full batch."""
+    return world * bt / (ms_per_step / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample of the same workload
 # ---------------------------------------------------------------------------
 def cpu_baseline(w, x_s, w_s, x_t, w_t, labels, budget_s: float, block: int = 16):
@@ -277,12 +296,9 @@ def main():
     status = fl.fljsd_workspace_status(run.plan, run.workspace, stream)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    if dist:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_max(ms_total, dist, dev)
     ms_step = ms_total / args.steps
-    value = world * w.bt / (ms_step / 1e3)
+    value = whole_job_tokens_per_s(world, w.bt, ms_step)
 
     # ---- roofline of the dominant kernel (the tensor-core GEMM) ----
     peaks = _peaks()
@@ -380,14 +396,10 @@ def run_e2e(torch, run, w, x_s, w_s, x_t, w_t, labels, steps, dist, world, dev):
     t0 = time.perf_counter()
     for _ in range(steps):
         step()
-    ms = (time.perf_counter() - t0) * 1e3 / steps
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max((time.perf_counter() - t0) * 1e3 / steps, dist, dev)
     h2d = hx_s.numel() * hx_s.element_size() + hx_t.numel() * hx_t.element_size() + (
         0 if hlab is None else hlab.numel() * 8)
-    return {"value": round(world * w.bt / (ms / 1e3), 1), "unit": "tokens/s",
+    return {"value": round(whole_job_tokens_per_s(world, w.bt, ms), 1), "unit": "tokens/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": host_loss.numel() * 4,
             "what": "pinned-host X_s, X_t, labels -> device; fljsd_forward + fljsd_backward; "

@@ -187,7 +187,27 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
     if (BRANCH == 2 && !PREC && fabsf(ma_) < 64.f && fabsf(mb_) < 64.f) {
       const float oa = ma_ + lda, ob = mb_ + ldb;
       float accq = 0.f, accp = 0.f;
-      for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+      const int64_t step = blockDim.x;
+      int64_t i = threadIdx.x;
+      // two vectors per iteration: four 16-byte loads in flight per thread
+      for (; i + step < nvec; i += 2 * step) {
+        float xs[N], xt[N], xs2[N], xt2[N];
+        V::load(zs + i * N, xs);
+        V::load(zt + i * N, xt);
+        V::load(zs + (i + step) * N, xs2);
+        V::load(zt + (i + step) * N, xt2);
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          float Q, P, xm, ym;
+          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          accq = fmaf(Q, xm, accq);
+          accp = fmaf(P, ym, accp);
+          lean_terms(xs2[k], xt2[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          accq = fmaf(Q, xm, accq);
+          accp = fmaf(P, ym, accp);
+        }
+      }
+      for (; i < nvec; i += step) {
         float xs[N], xt[N];
         V::load(zs + i * N, xs);
         V::load(zt + i * N, xt);
@@ -212,17 +232,35 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       // dz = ln2 * scale * Q * ((1-beta) xm - S)
       const float k0 = 0.6931471805599453f * w * a.inv_temperature * a.loss_scale;
       const float k1 = k0 * omb, k2 = k0 * S2;
-      for (int64_t i = nvec - 1 - threadIdx.x; i >= 0; i -= blockDim.x) {
+      int64_t i3 = nvec - 1 - threadIdx.x;
+      for (; i3 - step >= 0; i3 -= 2 * step) {
+        float xs[N], xt[N], xs2[N], xt2[N];
+        V::load(zs + i3 * N, xs);
+        V::load(zt + i3 * N, xt);
+        V::load(zs + (i3 - step) * N, xs2);
+        V::load(zt + (i3 - step) * N, xt2);
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          float Q, P, xm, ym;
+          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          xs[k] = Q * fmaf(k1, xm, -k2);
+          lean_terms(xs2[k], xt2[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          xs2[k] = Q * fmaf(k1, xm, -k2);
+        }
+        V::store(zs + i3 * N, xs);
+        V::store(zs + (i3 - step) * N, xs2);
+      }
+      for (; i3 >= 0; i3 -= step) {
         float xs[N], xt[N];
-        V::load(zs + i * N, xs);
-        V::load(zt + i * N, xt);
+        V::load(zs + i3 * N, xs);
+        V::load(zt + i3 * N, xt);
 #pragma unroll
         for (int k = 0; k < N; ++k) {
           float Q, P, xm, ym;
           lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
           xs[k] = Q * fmaf(k1, xm, -k2);
         }
-        V::store(zs + i * N, xs);
+        V::store(zs + i3 * N, xs);
       }
       for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
         float Q, P, xm, ym;
