@@ -54,7 +54,7 @@ typedef struct CUstream_st* fljsd_stream_t;
 typedef enum {
   FLJSD_OK = 0,
   FLJSD_ERR_INVALID_ARG = 1, /* null pointer, bad size, beta or temperature, misalignment */
-  FLJSD_ERR_UNSUPPORTED = 2, /* valid but not handled, e.g. bf16 with H % 8 != 0 */
+  FLJSD_ERR_UNSUPPORTED = 2, /* valid but beyond the kernels' limits (sizes above 2^30) */
   FLJSD_ERR_WORKSPACE = 3,   /* workspace smaller than the plan requires */
   FLJSD_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
   FLJSD_ERR_TIMEOUT = 5      /* a bounded device-side wait expired */
