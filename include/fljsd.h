@@ -216,13 +216,18 @@ fljsd_status fljsd_workspace_status(const fljsd_plan_t* plan, const void* worksp
  *   D stored [m x ldd]. All bf16, device, 16-byte aligned; lda, ldb, ldd
  *   multiples of 8; m, n, k >= 1.
  * status: device int32 that receives FLJSD_ERR_TIMEOUT if a bounded wait
- * expires (may be NULL). Asynchronous on `stream`. FLJSD_ERR_INVALID_ARG for
+ * expires (may be NULL). flags: 0 or FLJSD_GEMM_NO_MULTICAST (below).
+ * Asynchronous on `stream`. FLJSD_ERR_INVALID_ARG for
  * shapes or alignments outside the above.
  */
 fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const void* b,
                              int64_t ldb, int32_t b_mn, void* d, int64_t ldd, int64_t m,
                              int64_t n, int64_t k, int32_t accumulate, int32_t* status,
-                             fljsd_stream_t stream);
+                             int32_t flags, fljsd_stream_t stream);
+/* flags of fljsd_gemm_bf16: by default pairs of 128-row blocks of D run as
+ * 2-CTA clusters that fetch each B tile once for both (TMA multicast);
+ * FLJSD_GEMM_NO_MULTICAST runs one CTA per tile. The results are identical. */
+#define FLJSD_GEMM_NO_MULTICAST 1
 
 /*
  * Distances over given distributions (no GEMM). Both take [rows x v] row-major

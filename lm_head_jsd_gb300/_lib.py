@@ -78,7 +78,8 @@ def _load():
     lib.fljsd_workspace_status.restype = ctypes.c_int
     lib.fljsd_gemm_bf16.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, ctypes.c_int64,
                                     ctypes.c_int32, P, ctypes.c_int64, ctypes.c_int64,
-                                    ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, P, P]
+                                    ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, P,
+                                    ctypes.c_int32, P]
     lib.fljsd_gemm_bf16.restype = ctypes.c_int
     lib.fljsd_rows_workspace_bytes.argtypes = [ctypes.c_int64]
     lib.fljsd_rows_workspace_bytes.restype = ctypes.c_size_t
@@ -200,10 +201,13 @@ def fljsd_workspace_status(plan, workspace, stream=None) -> int:
     return out.value
 
 
+FLJSD_GEMM_NO_MULTICAST = 1
+
+
 def fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate=0, status=None,
-                    stream=None, check=True) -> int:
+                    flags=0, stream=None, check=True) -> int:
     st = lib.fljsd_gemm_bf16(_ptr(a), lda, a_mn, _ptr(b), ldb, b_mn, _ptr(d), ldd, m, n, k,
-                             accumulate, _ptr(status), _stream(stream))
+                             accumulate, _ptr(status), flags, _stream(stream))
     if check and st != FLJSD_OK:
         raise FljsdError(st, "fljsd_gemm_bf16")
     return st

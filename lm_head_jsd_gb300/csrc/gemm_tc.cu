@@ -110,6 +110,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Same copy, delivered to the same shared-memory offset (and completing on the
+// same mbarrier offset) in every CTA of the cluster named in cta_mask.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                               int32_t x, int32_t y, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // tcgen05 shared-memory matrix descriptor (sm_100 family):
 // [0,14) start >> 4, [16,30) leading-dimension byte offset >> 4,
 // [32,46) stride-dimension byte offset >> 4, [46,48) version = 1,
@@ -143,6 +163,14 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// Arrive on the mbarrier at this offset in every CTA of cta_mask once all
+// previously issued MMAs of this thread have completed.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
       : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -190,6 +218,9 @@ struct KParams {
   float2* stats;       // [m x num_n_blocks] (max, sum 2^(x - max)) per row and tile, or null
   float stats_scale;   // x = bf16(value) * stats_scale
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
+  // scheduling units: m-blocks (one CTA per tile) or pairs of m-blocks (a
+  // 2-CTA cluster per pair, sharing the B tile through multicast)
+  int m_units, num_units;
   int raster_n_fastest;
   int group_m;  // m-blocks per band in the grouped order
   int accumulate;
@@ -198,7 +229,7 @@ struct KParams {
   int* status;
 };
 
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, bool MC>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               __nv_bfloat16* __restrict__ D, KParams p) {
@@ -212,7 +243,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&cb->full[s]), 1);
-      mbar_init(smem_u32(&cb->empty[s]), 1);
+      // with multicast both CTAs' MMAs must have read a stage before either
+      // producer refills it (each producer writes into both CTAs)
+      mbar_init(smem_u32(&cb->empty[s]), MC ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&cb->tmem_full[a]), 1);
@@ -232,23 +265,31 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = cb->tmem_base;
+  // the peer's multicast copies and commits target this CTA's barriers: they
+  // must be initialised cluster-wide before anyone issues
+  if (MC) cluster_sync_all();
+  const uint32_t rank = MC ? cluster_ctarank() : 0u;
+  const int unit0 = MC ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int unit_step = MC ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   // Tile order. n-fastest: all n-blocks of a few m-blocks run together (used
   // when B is small and A streams). Grouped: bands of group_m m-blocks; inside
   // a band the m-blocks vary fastest and the band walks every n-block, so the
   // band's slice of A stays in L2 while B streams through once per band.
   auto tile_coords = [&](int t, int& mb, int& nb) {
+    int mu;
     if (p.raster_n_fastest) {
       nb = t % p.num_n_blocks;
-      mb = t / p.num_n_blocks;
+      mu = t / p.num_n_blocks;
     } else {
       const int band = t / (p.group_m * p.num_n_blocks);
       const int m0 = band * p.group_m;
-      const int gm = min(p.group_m, p.num_m_blocks - m0);
+      const int gm = min(p.group_m, p.m_units - m0);
       const int r = t - band * p.group_m * p.num_n_blocks;
-      mb = m0 + r % gm;
+      mu = m0 + r % gm;
       nb = r / gm;
     }
+    mb = MC ? 2 * mu + (int)rank : mu;
   };
 
   if (warp == 0) {
@@ -260,7 +301,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = unit0; ok && t < p.num_units; t += unit_step) {
         int mb, nb;
         tile_coords(t, mb, nb);
         const int m0 = mb * BM, n0 = nb * BN;
@@ -280,7 +321,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           } else {
             tma_load_2d(sa, &tmA, fb, k0, m0);
           }
-          if (B_MN) {
+          if (MC) {
+            // this CTA fetches half of the B tile for both CTAs of the pair
+            if (B_MN) {
+#pragma unroll
+              for (int j = 2 * (int)rank; j < 2 * (int)rank + 2; ++j)
+                tma_load_2d_mc(sb + j * 8192, &tmB, fb, n0 + 64 * j, k0, (uint16_t)3);
+            } else {
+              tma_load_2d_mc(sb + rank * (B_BYTES / 2), &tmB, fb, k0, n0 + (int)rank * (BN / 2),
+                             (uint16_t)3);
+            }
+          } else if (B_MN) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tmB, fb, n0 + 64 * j, k0);
           } else {
@@ -307,7 +358,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int local = 0;
       bool ok = true;
       bool any = false;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+      for (int t = unit0; ok && t < p.num_units; t += unit_step, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!wait_bar(cb, smem_u32(&cb->tmem_empty[acc]), acc_phase ^ 1u, p.status)) break;
@@ -334,7 +385,11 @@ __global__ void __launch_bounds__(THREADS, 1)
               bd = smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
             mma_bf16(tmem_d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(smem_u32(&cb->empty[stage]));  // frees the stage once read
+          // frees the stage once read (in both CTAs of a multicast pair)
+          if (MC)
+            mma_commit_mc(smem_u32(&cb->empty[stage]), (uint16_t)3);
+          else
+            mma_commit(smem_u32(&cb->empty[stage]));
           any = true;
           if (++stage == STAGES) {
             stage = 0;
@@ -354,7 +409,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- epilogue (warps 2..5) ----------------
     const int sub = warp & 3;  // TMEM lane quarter this warp may access
     int local = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+    for (int t = unit0; t < p.num_units; t += unit_step, ++local) {
       int mb, nb;
       tile_coords(t, mb, nb);
       const int acc = local & 1;
@@ -467,6 +522,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // no CTA of a pair leaves while its peer may still write into its shared
+  // memory or arrive on its barriers
+  if (MC) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -506,20 +564,50 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int
   return r == CUDA_SUCCESS;
 }
 
-template <bool A_MN, bool B_MN>
-cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, __nv_bfloat16* d,
-                     const KParams& p, cudaStream_t st) {
+template <bool A_MN, bool B_MN, bool MC>
+cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, __nv_bfloat16* d, KParams p,
+                     cudaStream_t st) {
+  static int max_clusters[64] = {0};
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<A_MN, B_MN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  const bool cache = dev >= 0 && dev < 64;
+  auto kern = k_gemm_tc<A_MN, B_MN, MC>;
+  if (!cache || !attr_set[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (cache) attr_set[dev] = true;
   }
-  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  k_gemm_tc<A_MN, B_MN><<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, d, p);
+  if (!MC) {
+    const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
+    kern<<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, d, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // a persistent grid must not exceed the clusters that can be resident at once
+  if (!cache || max_clusters[dev] == 0) {
+    int n = 0;
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = 1;
+    if (cache) max_clusters[dev] = n;
+    else max_clusters[0] = n;
+  }
+  const int mc = cache ? max_clusters[dev] : max_clusters[0];
+  const int clusters = p.num_units < mc ? p.num_units : mc;
+  cfg.gridDim = dim3(2 * clusters);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, d, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -534,6 +622,10 @@ bool tc_gemm_supported(const TcGemmArgs& g) {
 
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   if (!tc_gemm_supported(g)) return cudaErrorInvalidValue;
+  // pairs of m-blocks share B through a 2-CTA cluster whenever there are two
+  // m-blocks to pair (and g.no_multicast is not set)
+  const int64_t mblocks = (g.m + BM - 1) / BM;
+  const bool mc = mblocks >= 2 && !g.no_multicast;
   CUtensorMap ma, mb;
   bool ok;
   if (g.a_mn)  // A stored [k x m]
@@ -543,28 +635,30 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   if (!ok) return cudaErrorInvalidValue;
   if (g.b_mn)  // B stored [k x n]
     ok = make_map(&mb, g.b, g.n, g.k, g.ldb, 64, 64);
-  else  // B stored [n x k]
-    ok = make_map(&mb, g.b, g.k, g.n, g.ldb, BK, BN);
+  else  // B stored [n x k]; with multicast each CTA fetches half the tile's rows
+    ok = make_map(&mb, g.b, g.k, g.n, g.ldb, BK, mc ? BN / 2 : BN);
   if (!ok) return cudaErrorInvalidValue;
   KParams p{};
   p.m = g.m;
   p.n = g.n;
   p.k = g.k;
   p.ldd = g.ldd;
-  p.num_m_blocks = (int)((g.m + BM - 1) / BM);
+  p.num_m_blocks = (int)mblocks;
   p.num_n_blocks = (int)((g.n + BN - 1) / BN);
   p.num_k_blocks = (int)((g.k + BK - 1) / BK);
   const int64_t tiles = (int64_t)p.num_m_blocks * p.num_n_blocks;
   if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
   p.num_tiles = (int)tiles;
+  p.m_units = mc ? (p.num_m_blocks + 1) / 2 : p.num_m_blocks;
+  p.num_units = p.m_units * p.num_n_blocks;
   p.raster_n_fastest = g.raster_n_fastest;
-  // band of A rows whose K extent stays around 16 MB (at least one m-block)
+  // band of A rows whose K extent stays around 16 MB (at least one unit)
   {
     const int64_t band_bytes = 16ll << 20;
-    const int64_t per_mblock = (int64_t)BM * g.k * 2;
-    int64_t gm = per_mblock > 0 ? band_bytes / per_mblock : 1;
+    const int64_t per_unit = (int64_t)BM * (mc ? 2 : 1) * g.k * 2;
+    int64_t gm = per_unit > 0 ? band_bytes / per_unit : 1;
     if (gm < 1) gm = 1;
-    if (gm > p.num_m_blocks) gm = p.num_m_blocks;
+    if (gm > p.m_units) gm = p.m_units;
     p.group_m = (int)gm;
   }
   p.accumulate = g.accumulate;
@@ -574,10 +668,16 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.stats = g.stats;
   p.stats_scale = g.stats_scale;
   auto* d = reinterpret_cast<__nv_bfloat16*>(g.d);
-  if (!g.a_mn && !g.b_mn) return launch_t<false, false>(ma, mb, d, p, st);
-  if (!g.a_mn && g.b_mn) return launch_t<false, true>(ma, mb, d, p, st);
-  if (g.a_mn && g.b_mn) return launch_t<true, true>(ma, mb, d, p, st);
-  return launch_t<true, false>(ma, mb, d, p, st);
+  if (mc) {
+    if (!g.a_mn && !g.b_mn) return launch_t<false, false, true>(ma, mb, d, p, st);
+    if (!g.a_mn && g.b_mn) return launch_t<false, true, true>(ma, mb, d, p, st);
+    if (g.a_mn && g.b_mn) return launch_t<true, true, true>(ma, mb, d, p, st);
+    return launch_t<true, false, true>(ma, mb, d, p, st);
+  }
+  if (!g.a_mn && !g.b_mn) return launch_t<false, false, false>(ma, mb, d, p, st);
+  if (!g.a_mn && g.b_mn) return launch_t<false, true, false>(ma, mb, d, p, st);
+  if (g.a_mn && g.b_mn) return launch_t<true, true, false>(ma, mb, d, p, st);
+  return launch_t<true, false, false>(ma, mb, d, p, st);
 }
 
 }  // namespace fljsd

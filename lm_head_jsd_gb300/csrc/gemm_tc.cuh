@@ -32,6 +32,7 @@ struct TcGemmArgs {
   // touched, unless finalize == 1: then D = round(d32 + product).
   float* d32;
   int finalize;
+  int no_multicast;  // 1: one CTA per tile even where a 2-CTA cluster could share B
 };
 
 constexpr int TC_TILE_N = 256;

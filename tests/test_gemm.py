@@ -29,9 +29,10 @@ def _ref(a, a_mn, b, b_mn):
     return A @ B.t()
 
 
+@pytest.mark.parametrize("flags", [0, 1], ids=["pairs", "single"])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_gemm_layouts(a_mn, b_mn, shape):
+def test_gemm_layouts(a_mn, b_mn, shape, flags):
     from lm_head_jsd_gb300 import fljsd_gemm_bf16
 
     m, n, k = shape
@@ -42,7 +43,7 @@ def test_gemm_layouts(a_mn, b_mn, shape):
     dbuf = torch.empty(m, ldd, dtype=torch.bfloat16, device="cuda")
     d = dbuf[:, :n]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, 0, status)
+    fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, 0, status, flags)
     torch.cuda.synchronize()
     assert status.item() == 0
     ref = _ref(a, a_mn, b, b_mn)
@@ -50,7 +51,7 @@ def test_gemm_layouts(a_mn, b_mn, shape):
     assert err < 4e-3, float(err)
     # accumulate: D = D + A.B^T
     d0 = d.clone()
-    fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, 1, status)
+    fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, 1, status, flags)
     torch.cuda.synchronize()
     ref2 = d0.float() + ref
     err = (d.float() - ref2).norm() / ref2.norm()
@@ -82,3 +83,23 @@ def test_gemm_rejects_bad_arguments():
     assert fljsd_gemm_bf16(a, 16, 0, a, 16, 0, a, 16, 16, 16, 0, check=False) == 1  # k = 0
     assert fljsd_gemm_bf16(a, 12, 0, a, 16, 0, a, 16, 16, 16, 12, check=False) == 1  # lda % 8
     assert fljsd_gemm_bf16(a, 16, 2, a, 16, 0, a, 16, 16, 16, 16, check=False) == 1
+    assert fljsd_gemm_bf16(a, 16, 0, a, 16, 0, a, 16, 16, 16, 16, flags=4, check=False) == 1
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
+def test_gemm_pairs_and_single_ctas_agree_bitwise(a_mn, b_mn):
+    """Sharing B through multicast changes where the bytes come from, not the
+    arithmetic: both schedules give identical results (odd m-block count)."""
+    from lm_head_jsd_gb300 import fljsd_gemm_bf16
+
+    m, n, k = 1000, 777, 300
+    g = torch.Generator(device="cuda").manual_seed(11)
+    a, lda = _operand(a_mn, k if a_mn else m, m if a_mn else k, g)
+    b, ldb = _operand(b_mn, k if b_mn else n, n if b_mn else k, g)
+    ldd = -(-n // 8) * 8
+    d0 = torch.empty(m, ldd, dtype=torch.bfloat16, device="cuda")
+    d1 = torch.empty(m, ldd, dtype=torch.bfloat16, device="cuda")
+    fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d0, ldd, m, n, k, 0, None, 0)
+    fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d1, ldd, m, n, k, 0, None, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(d0[:, :n], d1[:, :n])
