@@ -226,7 +226,9 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
                              int32_t flags, fljsd_stream_t stream);
 /* flags of fljsd_gemm_bf16: by default pairs of 128-row blocks of D run as
  * 2-CTA clusters that fetch each B tile once for both (TMA multicast);
- * FLJSD_GEMM_NO_MULTICAST runs one CTA per tile. The results are identical. */
+ * FLJSD_GEMM_NO_MULTICAST runs one CTA per tile. The results are identical.
+ * The environment variable FLJSD_GEMM_MULTICAST=0 selects one CTA per tile for
+ * every GEMM of the library (read at each launch). */
 #define FLJSD_GEMM_NO_MULTICAST 1
 
 /*

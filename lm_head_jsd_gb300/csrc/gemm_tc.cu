@@ -24,6 +24,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 namespace fljsd {
@@ -625,7 +626,11 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   // pairs of m-blocks share B through a 2-CTA cluster whenever there are two
   // m-blocks to pair (and g.no_multicast is not set)
   const int64_t mblocks = (g.m + BM - 1) / BM;
-  const bool mc = mblocks >= 2 && !g.no_multicast;
+  // FLJSD_GEMM_MULTICAST=0 in the environment selects one CTA per tile for
+  // every call (both schedules compute identical results)
+  const char* env = getenv("FLJSD_GEMM_MULTICAST");
+  const bool env_off = env != nullptr && env[0] == '0';
+  const bool mc = mblocks >= 2 && !g.no_multicast && !env_off;
   CUtensorMap ma, mb;
   bool ok;
   if (g.a_mn)  // A stored [k x m]
