@@ -257,13 +257,13 @@ cudaError_t ce_gemm(int dtype, int kind, const void* a, int64_t lda, int a_mn, c
                     int64_t ldb, int b_mn, void* d, int64_t ldd, int64_t m, int64_t n, int64_t k,
                     int accumulate, int raster_n_fastest, int* status, cudaStream_t st,
                     float2* stats, float stats_scale, bool* stats_done, float* d32,
-                    int finalize) {
+                    int finalize, int no_multicast = 0) {
   if (stats_done) *stats_done = false;
   if (m <= 0 || n <= 0) return cudaSuccess;
   cudaError_t e;
   trace_begin(kind, st);
   TcGemmArgs t{a,      lda,   a_mn,        b,   ldb,     b_mn, d, ldd, m, n, k, accumulate,
-               raster_n_fastest, status, stats, stats_scale, d32, finalize};
+               raster_n_fastest, status, stats, stats_scale, d32, finalize, no_multicast};
   if (dtype == FLJSD_BF16 && tc_gemm_supported(t)) {
     e = launch_gemm_tc(t, st);
     if (stats_done) *stats_done = stats != nullptr;
@@ -377,7 +377,7 @@ fljsd_status fljsd_ce_forward(const fljsd_ce_problem* p, const fljsd_plan_t* pla
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
     e = ce_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_INPUT, z, L.ld, 0, w, p->h, 1,
                 static_cast<char*>(grad_input) + (size_t)r0 * p->h * s, p->h, rows, p->h, p->v,
-                0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0);
+                0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0, 1);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
     const bool last = r0 + rows >= p->bt;
     e = ce_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_WEIGHT, z, L.ld, 1, xc, p->h, 1, grad_weight,

@@ -139,13 +139,14 @@ cudaError_t run_gemm(int dtype, int kind, const void* a, int64_t lda, int a_mn, 
                      int64_t ldb, int b_mn, void* d, int64_t ldd, int64_t m, int64_t n, int64_t k,
                      int accumulate, int raster_n_fastest, int* status, cudaStream_t st,
                      float2* stats = nullptr, float stats_scale = 0.f,
-                     bool* stats_done = nullptr, float* d32 = nullptr, int finalize = 0) {
+                     bool* stats_done = nullptr, float* d32 = nullptr, int finalize = 0,
+                     int no_multicast = 0) {
   if (stats_done) *stats_done = false;
   if (m <= 0 || n <= 0) return cudaSuccess;
   cudaError_t e;
   trace_begin(kind, st);
   TcGemmArgs t{a,      lda,   a_mn,        b,   ldb,     b_mn, d, ldd, m, n, k, accumulate,
-               raster_n_fastest, status, stats, stats_scale, d32, finalize};
+               raster_n_fastest, status, stats, stats_scale, d32, finalize, no_multicast};
   if (dtype == FLJSD_BF16 && tc_gemm_supported(t)) {
     e = launch_gemm_tc(t, st);
     if (stats_done) *stats_done = stats != nullptr;
@@ -289,9 +290,10 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
     // grad_input rows of this chunk = dZ . W_s (W_s stored [V x H]: B is N-major)
+    // (measured: sharing W through multicast does not pay for this one)
     e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_INPUT, zs, L.ld, 0, w_s, p->h_s, 1,
                  static_cast<char*>(grad_input) + (size_t)r0 * p->h_s * s, p->h_s, rows, p->h_s,
-                 p->v, 0, 1, status, stream);
+                 p->v, 0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0, 1);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
     // grad_weight (+)= dZ^T . X_s: both operands stored with the chunk rows as
