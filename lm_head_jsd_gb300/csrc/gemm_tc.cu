@@ -456,6 +456,54 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           st_d += acc_d;
         }
+        // Read-modify-write of the stored value: issue the reads of the whole
+        // 32-column chunk before using any of them (they are independent).
+        const bool full_chunk = col0 + 32 <= p.n;
+        const bool rmw16 = p.accumulate && p.d32 == nullptr;
+        const bool rmw32 = p.d32 != nullptr && (p.accumulate || p.finalize);
+        if (full_chunk && (rmw16 || rmw32)) {
+          if (rmw16) {
+            const uint4* src = reinterpret_cast<const uint4*>(drow + col0);
+            uint4 o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[q] = src[q];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t ow[4] = {o[q].x, o[q].y, o[q].z, o[q].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v[q * 8 + 2 * e] += bf16_lo(ow[e]);
+                v[q * 8 + 2 * e + 1] += bf16_hi(ow[e]);
+              }
+            }
+          } else {
+            const float4* src = reinterpret_cast<const float4*>(p.d32 + row * p.ldd + col0);
+            float4 o[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o[q] = src[q];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              v[4 * q] += o[q].x;
+              v[4 * q + 1] += o[q].y;
+              v[4 * q + 2] += o[q].z;
+              v[4 * q + 3] += o[q].w;
+            }
+          }
+          if (p.d32 != nullptr && !p.finalize) {
+            float4* dst = reinterpret_cast<float4*>(p.d32 + row * p.ldd + col0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(drow + col0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack_bf16(v[q * 8], v[q * 8 + 1]), pack_bf16(v[q * 8 + 2], v[q * 8 + 3]),
+                                  pack_bf16(v[q * 8 + 4], v[q * 8 + 5]),
+                                  pack_bf16(v[q * 8 + 6], v[q * 8 + 7]));
+          }
+          continue;
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int64_t col = col0 + q * 8;
