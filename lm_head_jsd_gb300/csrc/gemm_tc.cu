@@ -705,9 +705,14 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.m_units = mc ? (p.num_m_blocks + 1) / 2 : p.num_m_blocks;
   p.num_units = p.m_units * p.num_n_blocks;
   p.raster_n_fastest = g.raster_n_fastest;
-  // band of A rows whose K extent stays around 16 MB (at least one unit)
+  // band of A rows whose K extent stays around 16 MB (at least one unit);
+  // FLJSD_GEMM_BAND_MB overrides the size
   {
-    const int64_t band_bytes = 16ll << 20;
+    int64_t band_bytes = 16ll << 20;
+    if (const char* b = getenv("FLJSD_GEMM_BAND_MB")) {
+      const long mb = strtol(b, nullptr, 10);
+      if (mb > 0 && mb <= 4096) band_bytes = (int64_t)mb << 20;
+    }
     const int64_t per_unit = (int64_t)BM * (mc ? 2 : 1) * g.k * 2;
     int64_t gm = per_unit > 0 ? band_bytes / per_unit : 1;
     if (gm < 1) gm = 1;
