@@ -222,8 +222,9 @@ struct KParams {
   // scheduling units: m-blocks (one CTA per tile) or pairs of m-blocks (a
   // 2-CTA cluster per pair, sharing the B tile through multicast)
   int m_units, num_units;
-  int raster_n_fastest;
-  int group_m;  // m-blocks per band in the grouped order
+  int raster;   // 0: bands of group_m m-units; 1: n-blocks fastest; 2: group_m x group_n blocks
+  int group_m;  // m-units per band / block
+  int group_n;  // n-blocks per block (raster 2)
   int accumulate;
   float* d32;    // optional fp32 accumulator with row stride ldd (see TcGemmArgs)
   int finalize;
@@ -279,9 +280,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   // band's slice of A stays in L2 while B streams through once per band.
   auto tile_coords = [&](int t, int& mb, int& nb) {
     int mu;
-    if (p.raster_n_fastest) {
+    if (p.raster == 1) {
       nb = t % p.num_n_blocks;
       mu = t / p.num_n_blocks;
+    } else if (p.raster == 2) {
+      // blocks of group_m x group_n tiles (about one wave each), n-bands outer
+      const int per_nband = p.m_units * p.group_n;
+      const int nband = t / per_nband;
+      const int n0 = nband * p.group_n;
+      const int gn = min(p.group_n, p.num_n_blocks - n0);
+      int r = t - nband * per_nband;
+      const int mband = r / (p.group_m * gn);
+      const int m0 = mband * p.group_m;
+      const int gm = min(p.group_m, p.m_units - m0);
+      r -= mband * p.group_m * gn;
+      mu = m0 + r % gm;
+      nb = n0 + r / gm;
     } else {
       const int band = t / (p.group_m * p.num_n_blocks);
       const int m0 = band * p.group_m;
@@ -704,20 +718,33 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.num_tiles = (int)tiles;
   p.m_units = mc ? (p.num_m_blocks + 1) / 2 : p.num_m_blocks;
   p.num_units = p.m_units * p.num_n_blocks;
-  p.raster_n_fastest = g.raster_n_fastest;
-  // band of A rows whose K extent stays around 16 MB (at least one unit);
-  // FLJSD_GEMM_BAND_MB overrides the size
-  {
-    int64_t band_bytes = 16ll << 20;
+  p.raster = g.raster_n_fastest;
+  if (const char* r = getenv("FLJSD_GEMM_RASTER")) {
+    if (r[0] >= '0' && r[0] <= '2' && p.raster != 0) p.raster = r[0] - '0';
+  }
+  if (p.raster == 2) {
+    // about one wave per block: 8 n-blocks wide, as many m-units as the
+    // resident CTAs (or pairs) cover
+    const int resident = mc ? num_sms() / 2 : num_sms();
+    p.group_n = p.num_n_blocks < 8 ? p.num_n_blocks : 8;
+    int gm = resident / (p.group_n > 0 ? p.group_n : 1);
+    if (gm < 1) gm = 1;
+    if (gm > p.m_units) gm = p.m_units;
+    p.group_m = gm;
+  } else {
+    // band of A rows whose K extent stays around 32 MB (at least one unit);
+    // FLJSD_GEMM_BAND_MB overrides the size
+    int64_t band_bytes = 32ll << 20;
     if (const char* b = getenv("FLJSD_GEMM_BAND_MB")) {
-      const long mb = strtol(b, nullptr, 10);
-      if (mb > 0 && mb <= 4096) band_bytes = (int64_t)mb << 20;
+      const long mbb = strtol(b, nullptr, 10);
+      if (mbb > 0 && mbb <= 4096) band_bytes = (int64_t)mbb << 20;
     }
     const int64_t per_unit = (int64_t)BM * (mc ? 2 : 1) * g.k * 2;
     int64_t gm = per_unit > 0 ? band_bytes / per_unit : 1;
     if (gm < 1) gm = 1;
     if (gm > p.m_units) gm = p.m_units;
     p.group_m = (int)gm;
+    p.group_n = p.num_n_blocks;
   }
   p.accumulate = g.accumulate;
   p.d32 = g.d32;

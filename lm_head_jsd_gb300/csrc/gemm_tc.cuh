@@ -19,7 +19,9 @@ struct TcGemmArgs {
   void* d; int64_t ldd;
   int64_t m, n, k;
   int accumulate;        // 1: D = D + A.B^T (fp32 add, one rounding)
-  int raster_n_fastest;  // tile order: 1 walks n-blocks fastest, 0 m-blocks fastest
+  // tile order: 0 = bands of m-blocks sweeping all n-blocks (A band stays in
+  // L2); 1 = n-blocks fastest; 2 = blocks of about one wave (8 n-blocks wide)
+  int raster_n_fastest;
   int* status;           // device word that receives FLJSD_ERR_TIMEOUT, or null
   // Optional row statistics of the stored output (requires accumulate == 0):
   // for row r and n-tile j (TC_TILE_N columns), stats[r * ceil(n / TC_TILE_N) + j]
