@@ -222,9 +222,8 @@ struct KParams {
   // scheduling units: m-blocks (one CTA per tile) or pairs of m-blocks (a
   // 2-CTA cluster per pair, sharing the B tile through multicast)
   int m_units, num_units;
-  int raster;   // 0: bands of group_m m-units; 1: n-blocks fastest; 2: group_m x group_n blocks
-  int group_m;  // m-units per band / block
-  int group_n;  // n-blocks per block (raster 2)
+  int raster;   // 0: bands of group_m m-units sweeping all n-blocks; 1: n-blocks fastest
+  int group_m;  // m-units per band
   int accumulate;
   float* d32;    // optional fp32 accumulator with row stride ldd (see TcGemmArgs)
   int finalize;
@@ -283,19 +282,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (p.raster == 1) {
       nb = t % p.num_n_blocks;
       mu = t / p.num_n_blocks;
-    } else if (p.raster == 2) {
-      // blocks of group_m x group_n tiles (about one wave each), n-bands outer
-      const int per_nband = p.m_units * p.group_n;
-      const int nband = t / per_nband;
-      const int n0 = nband * p.group_n;
-      const int gn = min(p.group_n, p.num_n_blocks - n0);
-      int r = t - nband * per_nband;
-      const int mband = r / (p.group_m * gn);
-      const int m0 = mband * p.group_m;
-      const int gm = min(p.group_m, p.m_units - m0);
-      r -= mband * p.group_m * gn;
-      mu = m0 + r % gm;
-      nb = n0 + r / gm;
     } else {
       const int band = t / (p.group_m * p.num_n_blocks);
       const int m0 = band * p.group_m;
@@ -719,21 +705,10 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.m_units = mc ? (p.num_m_blocks + 1) / 2 : p.num_m_blocks;
   p.num_units = p.m_units * p.num_n_blocks;
   p.raster = g.raster_n_fastest;
-  if (const char* r = getenv("FLJSD_GEMM_RASTER")) {
-    if (r[0] >= '0' && r[0] <= '2' && p.raster != 0) p.raster = r[0] - '0';
-  }
-  if (p.raster == 2) {
-    // about one wave per block: 8 n-blocks wide, as many m-units as the
-    // resident CTAs (or pairs) cover
-    const int resident = mc ? num_sms() / 2 : num_sms();
-    p.group_n = p.num_n_blocks < 8 ? p.num_n_blocks : 8;
-    int gm = resident / (p.group_n > 0 ? p.group_n : 1);
-    if (gm < 1) gm = 1;
-    if (gm > p.m_units) gm = p.m_units;
-    p.group_m = gm;
-  } else {
+  {
     // band of A rows whose K extent stays around 32 MB (at least one unit);
-    // FLJSD_GEMM_BAND_MB overrides the size
+    // FLJSD_GEMM_BAND_MB overrides the size. (Measured on the logits GEMM:
+    // 16 MB bands read W four times, 32 MB bands twice and 3% faster.)
     int64_t band_bytes = 32ll << 20;
     if (const char* b = getenv("FLJSD_GEMM_BAND_MB")) {
       const long mbb = strtol(b, nullptr, 10);
@@ -744,7 +719,6 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
     if (gm < 1) gm = 1;
     if (gm > p.m_units) gm = p.m_units;
     p.group_m = (int)gm;
-    p.group_n = p.num_n_blocks;
   }
   p.accumulate = g.accumulate;
   p.d32 = g.d32;

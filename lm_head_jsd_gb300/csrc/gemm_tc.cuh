@@ -19,8 +19,8 @@ struct TcGemmArgs {
   void* d; int64_t ldd;
   int64_t m, n, k;
   int accumulate;        // 1: D = D + A.B^T (fp32 add, one rounding)
-  // tile order: 0 = bands of m-blocks sweeping all n-blocks (A band stays in
-  // L2); 1 = n-blocks fastest; 2 = blocks of about one wave (8 n-blocks wide)
+  // tile order: 0 = bands of m-blocks sweeping all n-blocks (the band of A
+  // stays in L2 while B streams); 1 = n-blocks fastest
   int raster_n_fastest;
   int* status;           // device word that receives FLJSD_ERR_TIMEOUT, or null
   // Optional row statistics of the stored output (requires accumulate == 0):
