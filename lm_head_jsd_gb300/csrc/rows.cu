@@ -19,7 +19,7 @@ namespace {
 
 using namespace rowmath;
 
-constexpr int kRowThreads = 512;
+constexpr int kRowThreads = 1024;
 constexpr int kWarps = kRowThreads / 32;
 
 // ---- (max, sum of 2^(x - max)) pairs -----------------------------------------
@@ -100,48 +100,6 @@ __device__ __forceinline__ void lean_terms(float zs, float zt, float c, float oa
   const bool tie = X2 == Y2;
   xm = tie ? 0.f : X2 - lM;
   ym = tie ? 0.f : Y2 - lM;
-}
-
-// Eight bf16 elements of the student and teacher rows (one 16-byte word
-// each): accumulate sum Q (X - log M) and sum P (Y - log M).
-__device__ __forceinline__ void lean_accumulate(const uint4& ws, const uint4& wt, float c,
-                                                float oa, float ob, float beta, float omb,
-                                                float& accq, float& accp) {
-  const uint32_t s4[4] = {ws.x, ws.y, ws.z, ws.w};
-  const uint32_t t4[4] = {wt.x, wt.y, wt.z, wt.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    float Q, P, xm, ym;
-    lean_terms(__uint_as_float(s4[e] << 16), __uint_as_float(t4[e] << 16), c, oa, ob, beta, omb,
-               Q, P, xm, ym);
-    accq = fmaf(Q, xm, accq);
-    accp = fmaf(P, ym, accp);
-    lean_terms(__uint_as_float(s4[e] & 0xffff0000u), __uint_as_float(t4[e] & 0xffff0000u), c, oa,
-               ob, beta, omb, Q, P, xm, ym);
-    accq = fmaf(Q, xm, accq);
-    accp = fmaf(P, ym, accp);
-  }
-}
-
-// The dlogits of eight bf16 elements, packed back into one 16-byte word.
-__device__ __forceinline__ uint4 lean_grad(const uint4& ws, const uint4& wt, float c, float oa,
-                                           float ob, float beta, float omb, float k1, float k2) {
-  const uint32_t s4[4] = {ws.x, ws.y, ws.z, ws.w};
-  const uint32_t t4[4] = {wt.x, wt.y, wt.z, wt.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    float Q, P, xm, ym, g0, g1;
-    lean_terms(__uint_as_float(s4[e] << 16), __uint_as_float(t4[e] << 16), c, oa, ob, beta, omb,
-               Q, P, xm, ym);
-    g0 = Q * fmaf(k1, xm, -k2);
-    lean_terms(__uint_as_float(s4[e] & 0xffff0000u), __uint_as_float(t4[e] & 0xffff0000u), c, oa,
-               ob, beta, omb, Q, P, xm, ym);
-    g1 = Q * fmaf(k1, xm, -k2);
-    __nv_bfloat162 h = __floats2bfloat162_rn(g0, g1);
-    o[e] = *reinterpret_cast<uint32_t*>(&h);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 template <typename T, int BRANCH>
@@ -230,25 +188,37 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       const float oa = ma_ + lda, ob = mb_ + ldb;
       float accq = 0.f, accp = 0.f;
       const int64_t step = blockDim.x;
-      // software-pipelined: the raw 16-byte words of the next two vectors are
-      // in flight while the current two are computed
-      const uint4* ps = reinterpret_cast<const uint4*>(zs);
-      const uint4* pt = reinterpret_cast<const uint4*>(zt);
       int64_t i = threadIdx.x;
-      uint4 cs0, ct0, cs1, ct1;
-      const bool have0 = i < nvec, have1 = i + step < nvec;
-      if (have0) { cs0 = ps[i]; ct0 = pt[i]; }
-      if (have1) { cs1 = ps[i + step]; ct1 = pt[i + step]; }
+      // two vectors per iteration: four 16-byte loads in flight per thread
       for (; i + step < nvec; i += 2 * step) {
-        uint4 ns0, nt0, ns1, nt1;
-        const bool n0 = i + 2 * step < nvec, n1 = i + 3 * step < nvec;
-        if (n0) { ns0 = ps[i + 2 * step]; nt0 = pt[i + 2 * step]; }
-        if (n1) { ns1 = ps[i + 3 * step]; nt1 = pt[i + 3 * step]; }
-        lean_accumulate(cs0, ct0, cz, oa, ob, beta, omb, accq, accp);
-        lean_accumulate(cs1, ct1, cz, oa, ob, beta, omb, accq, accp);
-        cs0 = ns0; ct0 = nt0; cs1 = ns1; ct1 = nt1;
+        float xs[N], xt[N], xs2[N], xt2[N];
+        V::load(zs + i * N, xs);
+        V::load(zt + i * N, xt);
+        V::load(zs + (i + step) * N, xs2);
+        V::load(zt + (i + step) * N, xt2);
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          float Q, P, xm, ym;
+          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          accq = fmaf(Q, xm, accq);
+          accp = fmaf(P, ym, accp);
+          lean_terms(xs2[k], xt2[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          accq = fmaf(Q, xm, accq);
+          accp = fmaf(P, ym, accp);
+        }
       }
-      if (i < nvec) lean_accumulate(cs0, ct0, cz, oa, ob, beta, omb, accq, accp);
+      for (; i < nvec; i += step) {
+        float xs[N], xt[N];
+        V::load(zs + i * N, xs);
+        V::load(zt + i * N, xt);
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          float Q, P, xm, ym;
+          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          accq = fmaf(Q, xm, accq);
+          accp = fmaf(P, ym, accp);
+        }
+      }
       for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
         float Q, P, xm, ym;
         lean_terms(V::one(zs + j), V::one(zt + j), cz, oa, ob, beta, omb, Q, P, xm, ym);
@@ -262,22 +232,35 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       // dz = ln2 * scale * Q * ((1-beta) xm - S)
       const float k0 = 0.6931471805599453f * w * a.inv_temperature * a.loss_scale;
       const float k1 = k0 * omb, k2 = k0 * S2;
-      uint4* qs = reinterpret_cast<uint4*>(zs);
       int64_t i3 = nvec - 1 - threadIdx.x;
-      {
-        uint4 cs0, ct0, cs1, ct1;
-        if (i3 >= 0) { cs0 = qs[i3]; ct0 = pt[i3]; }
-        if (i3 - step >= 0) { cs1 = qs[i3 - step]; ct1 = pt[i3 - step]; }
-        for (; i3 - step >= 0; i3 -= 2 * step) {
-          uint4 ns0, nt0, ns1, nt1;
-          const bool n0 = i3 - 2 * step >= 0, n1 = i3 - 3 * step >= 0;
-          if (n0) { ns0 = qs[i3 - 2 * step]; nt0 = pt[i3 - 2 * step]; }
-          if (n1) { ns1 = qs[i3 - 3 * step]; nt1 = pt[i3 - 3 * step]; }
-          qs[i3] = lean_grad(cs0, ct0, cz, oa, ob, beta, omb, k1, k2);
-          qs[i3 - step] = lean_grad(cs1, ct1, cz, oa, ob, beta, omb, k1, k2);
-          cs0 = ns0; ct0 = nt0; cs1 = ns1; ct1 = nt1;
+      for (; i3 - step >= 0; i3 -= 2 * step) {
+        float xs[N], xt[N], xs2[N], xt2[N];
+        V::load(zs + i3 * N, xs);
+        V::load(zt + i3 * N, xt);
+        V::load(zs + (i3 - step) * N, xs2);
+        V::load(zt + (i3 - step) * N, xt2);
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          float Q, P, xm, ym;
+          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          xs[k] = Q * fmaf(k1, xm, -k2);
+          lean_terms(xs2[k], xt2[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          xs2[k] = Q * fmaf(k1, xm, -k2);
         }
-        if (i3 >= 0) qs[i3] = lean_grad(cs0, ct0, cz, oa, ob, beta, omb, k1, k2);
+        V::store(zs + i3 * N, xs);
+        V::store(zs + (i3 - step) * N, xs2);
+      }
+      for (; i3 >= 0; i3 -= step) {
+        float xs[N], xt[N];
+        V::load(zs + i3 * N, xs);
+        V::load(zt + i3 * N, xt);
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          float Q, P, xm, ym;
+          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          xs[k] = Q * fmaf(k1, xm, -k2);
+        }
+        V::store(zs + i3 * N, xs);
       }
       for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
         float Q, P, xm, ym;
