@@ -7,13 +7,21 @@
 //               128 x 256 x 16, accumulating in tensor memory; two 256-column
 //               accumulators so the epilogue of tile i overlaps the main loop
 //               of tile i+1. Warp 1 also allocates / frees the 512 TMEM columns.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, rounding to bf16 (or
-//               fp32 read-modify-write of the stored bf16 value for
-//               accumulation), 16-byte stores.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, rounding to bf16 with
+//               16-byte stores, or a read-modify-write of the stored value (bf16
+//               or an fp32 side accumulator) for accumulation, and optionally
+//               the per-row (max, sum 2^(x - max)) partials of the stored tile
+//               (pass 1 of the online softmax).
 // Operands may be K-major (the contraction dimension contiguous) or MN-major;
 // the three contractions of the fused-linear JSD need: logits = X . W^T
 // (both K-major), grad_input = dZ . W (B MN-major), grad_weight = dZ^T . X
 // (both MN-major).
+//
+// Pairs of m-blocks can run as a 2-CTA cluster that shares the B tile: each
+// CTA fetches half of it with a TMA multicast into both CTAs, each MMA frees a
+// stage in both CTAs with a multicast commit, and cluster barriers fence the
+// start and the exit. Tile orders: bands of m-blocks sweeping all n-blocks
+// (the band of A stays in L2 while B streams), or n-blocks fastest.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the kernel records
 // FLJSD_ERR_TIMEOUT in a device status word, stops issuing work, drains what

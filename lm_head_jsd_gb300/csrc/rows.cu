@@ -1,5 +1,5 @@
-// Row kernels of the fused-linear JSD: the three passes over the vocabulary,
-// the valid-row count, the final loss reduction and the backward scaling.
+// Row kernels of the fused-linear JSD: the passes over the vocabulary, the
+// valid-row count, the final loss reduction and the backward scaling.
 //
 // The three-pass structure follows "[Perf] Fuse log-softmax into
 // fused_linear_jsd kernel" (Liger-Kernel PR 1352), "Details": pass 1 builds
@@ -7,8 +7,10 @@
 // together (online softmax, Milakov & Gimelshein, Algorithm 3); pass 2
 // accumulates the per-row loss and the cross-column term dX_sum; pass 3
 // recomputes dX and writes the logit gradient over the student logits
-// buffer. Logits are read in the input dtype and widened at load; all math is
-// fp32 in registers; e^x is evaluated as 2^(x*log2 e) on the ex2 unit.
+// buffer. On the tensor-core path pass 1 runs in the logits GEMM's epilogue
+// and this kernel only combines its per-tile partials. Logits are read in the
+// input dtype and widened at load; all math is fp32 in registers; e^x is
+// evaluated as 2^(x*log2 e) (the ex2 unit for bf16, exp2f for fp32).
 #include "internal.cuh"
 #include "jsd_math.cuh"
 
