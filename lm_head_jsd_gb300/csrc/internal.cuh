@@ -49,10 +49,7 @@ struct JsdRowArgs {
 cudaError_t launch_count_valid(const int64_t* labels, int64_t bt, int64_t ignore_index,
                                int* n_valid, cudaStream_t st);
 cudaError_t launch_jsd_rows(int dtype, const JsdRowArgs& a, cudaStream_t st);
-// bf16, generalized branch, with the GEMM's pass-1 partials: a 4-CTA cluster
-// per row (rows_cluster.cu)
-bool jsd_rows_cluster_supported(const JsdRowArgs& a);
-cudaError_t launch_jsd_rows_cluster(const JsdRowArgs& a, cudaStream_t st);
+
 cudaError_t launch_reduce_loss(const float* loss_rows, int64_t bt, int64_t v, int reduction,
                                const int* n_valid, float* loss, cudaStream_t st);
 cudaError_t launch_scale(int dtype, void* p, int64_t n, const float* g, cudaStream_t st);

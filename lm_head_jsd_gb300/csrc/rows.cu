@@ -16,8 +16,6 @@
 
 #include <math_constants.h>
 
-#include <cstdlib>
-
 namespace fljsd {
 namespace {
 
@@ -409,15 +407,8 @@ cudaError_t launch_rows_dt(const JsdRowArgs& a, cudaStream_t st) {
 cudaError_t launch_jsd_rows(int dtype, const JsdRowArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
   trace_begin(FLJSD_KERNEL_JSD_ROWS, st);
-  // FLJSD_ROWS_CLUSTER=0 keeps the one-CTA-per-row kernel (same results)
-  const char* env = getenv("FLJSD_ROWS_CLUSTER");
-  const bool cluster_ok = !(env != nullptr && env[0] == '0');
-  cudaError_t e;
-  if (dtype == FLJSD_BF16 && cluster_ok && jsd_rows_cluster_supported(a))
-    e = launch_jsd_rows_cluster(a, st);
-  else
-    e = dtype == FLJSD_BF16 ? launch_rows_dt<__nv_bfloat16>(a, st)
-                            : launch_rows_dt<float>(a, st);
+  cudaError_t e = dtype == FLJSD_BF16 ? launch_rows_dt<__nv_bfloat16>(a, st)
+                                      : launch_rows_dt<float>(a, st);
   trace_end(FLJSD_KERNEL_JSD_ROWS, st);
   return e;
 }
