@@ -14,7 +14,10 @@
 #include "internal.cuh"
 #include "jsd_math.cuh"
 
+#include <cuda_fp16.h>
 #include <math_constants.h>
+
+#include <cstdlib>
 
 namespace fljsd {
 namespace {
@@ -22,6 +25,7 @@ namespace {
 using namespace rowmath;
 
 constexpr int kRowThreads = 1024;
+constexpr int64_t kCacheVecMax = 12800;  // 200 KB of fp16 (8 elements per vector)
 constexpr int kWarps = kRowThreads / 32;
 
 // ---- (max, sum of 2^(x - max)) pairs -----------------------------------------
@@ -111,6 +115,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
   constexpr int N = V::N;
   __shared__ MD sh_md[kWarps];
   __shared__ float2 sh_s[kWarps];
+  extern __shared__ uint4 xm_cache[];  // lean path: fp16 X - log M of cache_vec vectors
 
   const float c = a.scale_log2;  // log2(e) / T
   const float beta = a.beta, omb = 1.f - a.beta;
@@ -185,11 +190,38 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
     // fold into one fma per element (exact to 2^-18 in log2 units while the
     // row maxima are below 64, a constant per-row shift that the loss does not
     // feel at first order), and the per-element products accumulate with fmas:
-    // S = (1-beta) sum Q xm, L = beta sum P ym + S.
+    // S = (1-beta) sum Q xm, L = beta sum P ym + S. Pass 2 also keeps
+    // xm = X - log M (fp16) of the row's first `cache_vec` vectors in shared
+    // memory, so pass 3 needs only Q = 2^X there: one ex2 instead of three and
+    // no second read of the teacher logits.
     if (BRANCH == 2 && !PREC && fabsf(ma_) < 64.f && fabsf(mb_) < 64.f) {
       const float oa = ma_ + lda, ob = mb_ + ldb;
       float accq = 0.f, accp = 0.f;
       const int64_t step = blockDim.x;
+      const int64_t ncache = nvec < a.cache_vec ? nvec : a.cache_vec;
+      uint4* cache = reinterpret_cast<uint4*>(xm_cache);
+      auto pass2_vec = [&](const float (&xs)[N], const float (&xt)[N], int64_t v) {
+        float xm8[N];
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+          float Q, P, xm, ym;
+          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+          accq = fmaf(Q, xm, accq);
+          accp = fmaf(P, ym, accp);
+          xm8[k] = xm;
+        }
+        if (v < ncache) {
+          uint32_t h[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            // clamped into the fp16 range: where |xm| is that large Q is 0
+            __half2 t = __floats2half2_rn(fminf(fmaxf(xm8[2 * e], -6.0e4f), 6.0e4f),
+                                          fminf(fmaxf(xm8[2 * e + 1], -6.0e4f), 6.0e4f));
+            h[e] = *reinterpret_cast<uint32_t*>(&t);
+          }
+          cache[v] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+      };
       int64_t i = threadIdx.x;
       // two vectors per iteration: four 16-byte loads in flight per thread
       for (; i + step < nvec; i += 2 * step) {
@@ -198,28 +230,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
         V::load(zt + i * N, xt);
         V::load(zs + (i + step) * N, xs2);
         V::load(zt + (i + step) * N, xt2);
-#pragma unroll
-        for (int k = 0; k < N; ++k) {
-          float Q, P, xm, ym;
-          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
-          accq = fmaf(Q, xm, accq);
-          accp = fmaf(P, ym, accp);
-          lean_terms(xs2[k], xt2[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
-          accq = fmaf(Q, xm, accq);
-          accp = fmaf(P, ym, accp);
-        }
+        pass2_vec(xs, xt, i);
+        pass2_vec(xs2, xt2, i + step);
       }
       for (; i < nvec; i += step) {
         float xs[N], xt[N];
         V::load(zs + i * N, xs);
         V::load(zt + i * N, xt);
-#pragma unroll
-        for (int k = 0; k < N; ++k) {
-          float Q, P, xm, ym;
-          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
-          accq = fmaf(Q, xm, accq);
-          accp = fmaf(P, ym, accp);
-        }
+        pass2_vec(xs, xt, i);
       }
       for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
         float Q, P, xm, ym;
@@ -227,49 +245,53 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
         accq = fmaf(Q, xm, accq);
         accp = fmaf(P, ym, accp);
       }
-      const float2 tot = block_sum2(make_float2(accq, accp), sh_s);
+      const float2 tot = block_sum2(make_float2(accq, accp), sh_s);  // also orders the cache
       const float S2 = omb * tot.x;
       const float L2 = fmaf(beta, tot.y, S2);
       if (threadIdx.x == 0) a.loss_rows[grow] = 0.6931471805599453f * L2 * a.loss_scale;
       // dz = ln2 * scale * Q * ((1-beta) xm - S)
       const float k0 = 0.6931471805599453f * w * a.inv_temperature * a.loss_scale;
       const float k1 = k0 * omb, k2 = k0 * S2;
+      auto pass3_vec = [&](int64_t v) {
+        float xs[N];
+        V::load(zs + v * N, xs);
+        if (v < ncache) {
+          const uint4 hv = cache[v];
+          const uint32_t h[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 xm2 = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
+            const float X0 = __fmaf_rn(xs[2 * e], cz, -oa);
+            const float X1 = __fmaf_rn(xs[2 * e + 1], cz, -oa);
+            xs[2 * e] = ex2(X0) * fmaf(k1, xm2.x, -k2);
+            xs[2 * e + 1] = ex2(X1) * fmaf(k1, xm2.y, -k2);
+          }
+        } else {
+          float xt[N];
+          V::load(zt + v * N, xt);
+#pragma unroll
+          for (int k = 0; k < N; ++k) {
+            float Q, P, xm, ym;
+            lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
+            xs[k] = Q * fmaf(k1, xm, -k2);
+          }
+        }
+        V::store(zs + v * N, xs);
+      };
+      // walk the row backwards: the lines pass 2 read last are the likeliest
+      // to still be in L2
       int64_t i3 = nvec - 1 - threadIdx.x;
       for (; i3 - step >= 0; i3 -= 2 * step) {
-        float xs[N], xt[N], xs2[N], xt2[N];
-        V::load(zs + i3 * N, xs);
-        V::load(zt + i3 * N, xt);
-        V::load(zs + (i3 - step) * N, xs2);
-        V::load(zt + (i3 - step) * N, xt2);
-#pragma unroll
-        for (int k = 0; k < N; ++k) {
-          float Q, P, xm, ym;
-          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
-          xs[k] = Q * fmaf(k1, xm, -k2);
-          lean_terms(xs2[k], xt2[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
-          xs2[k] = Q * fmaf(k1, xm, -k2);
-        }
-        V::store(zs + i3 * N, xs);
-        V::store(zs + (i3 - step) * N, xs2);
+        pass3_vec(i3);
+        pass3_vec(i3 - step);
       }
-      for (; i3 >= 0; i3 -= step) {
-        float xs[N], xt[N];
-        V::load(zs + i3 * N, xs);
-        V::load(zt + i3 * N, xt);
-#pragma unroll
-        for (int k = 0; k < N; ++k) {
-          float Q, P, xm, ym;
-          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
-          xs[k] = Q * fmaf(k1, xm, -k2);
-        }
-        V::store(zs + i3 * N, xs);
-      }
+      for (; i3 >= 0; i3 -= step) pass3_vec(i3);
       for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
         float Q, P, xm, ym;
         lean_terms(V::one(zs + j), V::one(zt + j), cz, oa, ob, beta, omb, Q, P, xm, ym);
         V::put(zs + j, Q * fmaf(k1, xm, -k2));
       }
-      __syncthreads();
+      __syncthreads();  // the cache is rewritten by the next row's pass 2
       continue;
     }
 
@@ -387,11 +409,32 @@ __global__ void k_scale(T* p, int64_t n, const float* gp) {
 }
 
 template <typename T, int BRANCH>
-cudaError_t launch_rows_t(const JsdRowArgs& a, cudaStream_t st) {
+cudaError_t launch_rows_t(JsdRowArgs a, cudaStream_t st) {
   // One row in flight per SM keeps the rows between pass 2 and pass 3 small
-  // enough for L2 (148 rows of 2 x 256 KB at V = 128256 in bf16).
+  // enough for L2 (152 rows of 2 x 256 KB at V = 128256 in bf16).
   const int64_t grid = a.rows < (int64_t)num_sms() ? a.rows : (int64_t)num_sms();
-  k_jsd_rows<T, BRANCH><<<(unsigned)grid, kRowThreads, 0, st>>>(a);
+  size_t smem = 0;
+  a.cache_vec = 0;
+  if (BRANCH == 2 && sizeof(T) == 2) {
+    // up to 200 KB of fp16 X - log M per row (12800 vectors of 8 elements)
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(k_jsd_rows<T, BRANCH>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kCacheVecMax * 16);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    const int64_t nvec = a.v / 8;
+    a.cache_vec = nvec < kCacheVecMax ? nvec : kCacheVecMax;
+    // FLJSD_ROWS_CACHE=0 recomputes every element in pass 3 instead
+    if (const char* env = getenv("FLJSD_ROWS_CACHE"))
+      if (env[0] == '0') a.cache_vec = 0;
+    smem = (size_t)a.cache_vec * 16;
+  }
+  k_jsd_rows<T, BRANCH><<<(unsigned)grid, kRowThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
