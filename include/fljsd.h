@@ -230,6 +230,10 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
  * The environment variable FLJSD_GEMM_MULTICAST=0 selects one CTA per tile for
  * every GEMM of the library (read at each launch). */
 #define FLJSD_GEMM_NO_MULTICAST 1
+/* Test of the failure path: the kernel's copy warp issues nothing, so its
+ * first bounded wait expires after 50 ms; *status then holds
+ * FLJSD_ERR_TIMEOUT, D is not written, and the context stays usable. */
+#define FLJSD_GEMM_TEST_STALL 2
 
 /*
  * Distances over given distributions (no GEMM). Both take [rows x v] row-major

@@ -202,6 +202,7 @@ def fljsd_workspace_status(plan, workspace, stream=None) -> int:
 
 
 FLJSD_GEMM_NO_MULTICAST = 1
+FLJSD_GEMM_TEST_STALL = 2
 
 
 def fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate=0, status=None,

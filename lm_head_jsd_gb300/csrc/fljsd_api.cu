@@ -351,13 +351,16 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
                              int64_t ldb, int32_t b_mn, void* d, int64_t ldd, int64_t m,
                              int64_t n, int64_t k, int32_t accumulate, int32_t* status,
                              int32_t flags, fljsd_stream_t stream_) {
-  if ((flags & ~FLJSD_GEMM_NO_MULTICAST) != 0) return FLJSD_ERR_INVALID_ARG;
+  if ((flags & ~(FLJSD_GEMM_NO_MULTICAST | FLJSD_GEMM_TEST_STALL)) != 0)
+    return FLJSD_ERR_INVALID_ARG;
   if (!a || !b || !d || m <= 0 || n <= 0 || k <= 0) return FLJSD_ERR_INVALID_ARG;
   if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1) || (accumulate != 0 && accumulate != 1))
     return FLJSD_ERR_INVALID_ARG;
   if (lda < (a_mn ? m : k) || ldb < (b_mn ? n : k) || ldd < n) return FLJSD_ERR_INVALID_ARG;
+  const bool stall = (flags & FLJSD_GEMM_TEST_STALL) != 0;
   TcGemmArgs t{a,       lda,  a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, 1, status,
-               nullptr, 0.f,  nullptr, 0, (flags & FLJSD_GEMM_NO_MULTICAST) ? 1 : 0};
+               nullptr, 0.f,  nullptr, 0, (flags & FLJSD_GEMM_NO_MULTICAST) ? 1 : 0,
+               stall ? 50ull * 1000 * 1000 : 0ull, stall ? 1 : 0};
   if (!tc_gemm_supported(t)) return FLJSD_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   trace_begin(FLJSD_KERNEL_SMALL, stream);

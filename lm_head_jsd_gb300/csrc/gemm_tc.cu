@@ -47,7 +47,7 @@ constexpr int ACC_COLS = BN;                    // fp32 accumulator columns per 
 constexpr int TMEM_COLS = 2 * ACC_COLS;         // double-buffered accumulator
 constexpr int THREADS = 192;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr unsigned long long kTimeoutNs = 10ull * 1000 * 1000 * 1000;  // 10 s
+constexpr unsigned long long kTimeoutNs = 10ull * 1000 * 1000 * 1000;  // 10 s by default
 
 // ---- PTX wrappers -----------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -87,6 +87,7 @@ struct Ctrl {
   unsigned long long tmem_full[2];
   unsigned long long tmem_empty[2];
   unsigned long long drain;
+  unsigned long long timeout_ns;
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -101,7 +102,7 @@ __device__ __forceinline__ bool wait_bar(Ctrl* cb, uint32_t bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 63u) {
       if (cb->abort) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
+      if (globaltimer() - t0 > cb->timeout_ns) {
         cb->abort = 1;
         if (status) atomicExch(status, (int)FLJSD_ERR_TIMEOUT);
         return false;
@@ -235,6 +236,8 @@ struct KParams {
   int accumulate;
   float* d32;    // optional fp32 accumulator with row stride ldd (see TcGemmArgs)
   int finalize;
+  unsigned long long timeout_ns;  // limit of every mbarrier wait
+  int stall_producer;             // test of the bounded waits: issue no copies
   int* status;
 };
 
@@ -262,6 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(smem_u32(&cb->drain), 1);
     cb->abort = 0;
+    cb->timeout_ns = p.timeout_ns;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t issued_parity[STAGES];
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false;
-      bool ok = true;
+      bool ok = !p.stall_producer;
       for (int t = unit0; ok && t < p.num_units; t += unit_step) {
         int mb, nb;
         tile_coords(t, mb, nb);
@@ -731,6 +735,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.accumulate = g.accumulate;
   p.d32 = g.d32;
   p.finalize = g.finalize;
+  p.timeout_ns = g.timeout_ns ? g.timeout_ns : kTimeoutNs;
+  p.stall_producer = g.stall_producer;
   p.status = g.status;
   p.stats = g.stats;
   p.stats_scale = g.stats_scale;

@@ -35,6 +35,11 @@ struct TcGemmArgs {
   float* d32;
   int finalize;
   int no_multicast;  // 1: one CTA per tile even where a 2-CTA cluster could share B
+  // Test of the bounded waits: with stall_producer no copy is issued, so the
+  // MMA's first wait expires after timeout_ns (0 = the 10 s default) and the
+  // kernel reports FLJSD_ERR_TIMEOUT in *status and exits cleanly.
+  unsigned long long timeout_ns;
+  int stall_producer;
 };
 
 constexpr int TC_TILE_N = 256;
