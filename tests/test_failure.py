@@ -38,7 +38,7 @@ def test_forward_reports_ok_in_the_workspace_status():
     from lm_head_jsd_gb300 import FusedLinearJSD, fljsd_workspace_status
 
     w = jsd_inputs.custom("status", 61, 256, 64, 3000, "bf16")
-    x_s, w_s, x_t, w_t, _ = (t.cuda() for t in jsd_inputs.make_inputs(w, "cpu")[:4]) + (None,)
+    x_s, w_s, x_t, w_t = (t.cuda() for t in jsd_inputs.make_inputs(w, "cpu")[:4])
     run = FusedLinearJSD(256, 64, 64, 3000, torch.bfloat16)
     run.forward(x_s, w_s, x_t, w_t)
     assert fljsd_workspace_status(run.plan, run.workspace) == 0
