@@ -213,7 +213,7 @@ inline bool aligned16(const void* q) { return ((uintptr_t)q & 15u) == 0; }
 
 struct CeLayout {
   int64_t ld, ntiles;
-  size_t z, stats, loss_rows, misc, acc32, total, logits_bytes, stats_bytes;
+  size_t z, stats, loss_rows, misc, acc32, splitk, splitk_bytes, total, logits_bytes, stats_bytes;
   bool use_acc32;
 };
 
@@ -229,7 +229,10 @@ CeLayout ce_layout(const fljsd_ce_problem& p, int64_t c) {
   L.misc = L.loss_rows + align_up((size_t)p.bt * sizeof(float));
   L.use_acc32 = (p.flags & FLJSD_FLAG_ACCUM_FP32) && p.dtype == FLJSD_BF16 && c < p.bt;
   L.acc32 = L.misc + kAlign;
-  L.total = L.acc32 + (L.use_acc32 ? align_up((size_t)p.v * (size_t)p.h * sizeof(float)) : 0);
+  L.splitk = L.acc32 + (L.use_acc32 ? align_up((size_t)p.v * (size_t)p.h * sizeof(float)) : 0);
+  // fp32 partials of a split grad_input contraction (chunks with few tiles)
+  L.splitk_bytes = p.dtype == FLJSD_BF16 && c > 0 ? align_up(tc_splitk_bytes(c, p.h, p.v, TC_PLAN_CTAS)) : 0;
+  L.total = L.splitk + L.splitk_bytes;
   L.logits_bytes = (size_t)c * (size_t)L.ld * dsize(p.dtype);
   L.stats_bytes = sb + align_up((size_t)p.bt * sizeof(float)) + kAlign;
   return L;
@@ -257,13 +260,16 @@ cudaError_t ce_gemm(int dtype, int kind, const void* a, int64_t lda, int a_mn, c
                     int64_t ldb, int b_mn, void* d, int64_t ldd, int64_t m, int64_t n, int64_t k,
                     int accumulate, int raster_n_fastest, int* status, cudaStream_t st,
                     float2* stats, float stats_scale, bool* stats_done, float* d32,
-                    int finalize, int no_multicast = 0) {
+                    int finalize, int no_multicast = 0, void* splitk_ws = nullptr,
+                    size_t splitk_bytes = 0) {
   if (stats_done) *stats_done = false;
   if (m <= 0 || n <= 0) return cudaSuccess;
   cudaError_t e;
   trace_begin(kind, st);
   TcGemmArgs t{a,      lda,   a_mn,        b,   ldb,     b_mn, d, ldd, m, n, k, accumulate,
                raster_n_fastest, status, stats, stats_scale, d32, finalize, no_multicast};
+  t.splitk_ws = static_cast<float*>(splitk_ws);
+  t.splitk_ws_bytes = splitk_bytes;
   if (dtype == FLJSD_BF16 && tc_gemm_supported(t)) {
     e = launch_gemm_tc(t, st);
     if (stats_done) *stats_done = stats != nullptr;
@@ -300,8 +306,10 @@ fljsd_status fljsd_ce_plan(const fljsd_ce_problem* p, size_t free_hbm_bytes, flj
     if (ce_layout(*p, p->bt).total <= budget) {
       c = p->bt;
     } else {
-      const size_t fixed = ce_layout(*p, 0).total;
-      const size_t per_row = ce_layout(*p, 1).total - fixed;
+      // per-row growth without the split-K scratch (which shrinks as chunks grow)
+      const CeLayout l0 = ce_layout(*p, 0), l1 = ce_layout(*p, 1);
+      const size_t fixed = l0.total;
+      const size_t per_row = (l1.total - l1.splitk_bytes) - (l0.total - l0.splitk_bytes);
       if (budget < fixed + per_row) return FLJSD_ERR_WORKSPACE;
       c = (int64_t)((budget - fixed) / (per_row ? per_row : 1));
       if (c >= 128) c = c / 128 * 128;
@@ -377,7 +385,8 @@ fljsd_status fljsd_ce_forward(const fljsd_ce_problem* p, const fljsd_plan_t* pla
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
     e = ce_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_INPUT, z, L.ld, 0, w, p->h, 1,
                 static_cast<char*>(grad_input) + (size_t)r0 * p->h * s, p->h, rows, p->h, p->v,
-                0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0, 1);
+                0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0, 1, ws + L.splitk,
+                L.splitk_bytes);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
     const bool last = r0 + rows >= p->bt;
     e = ce_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_WEIGHT, z, L.ld, 1, xc, p->h, 1, grad_weight,

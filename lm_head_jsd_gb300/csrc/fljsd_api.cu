@@ -49,6 +49,8 @@ void trace_begin(int kind, cudaStream_t st) {
   g_trace.open = i;
 }
 
+void count_extra_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 void trace_end(int kind, cudaStream_t st) {
   if (g_trace.max == 0) return;
   std::lock_guard<std::mutex> lk(g_trace.mu);
@@ -140,13 +142,15 @@ cudaError_t run_gemm(int dtype, int kind, const void* a, int64_t lda, int a_mn, 
                      int accumulate, int raster_n_fastest, int* status, cudaStream_t st,
                      float2* stats = nullptr, float stats_scale = 0.f,
                      bool* stats_done = nullptr, float* d32 = nullptr, int finalize = 0,
-                     int no_multicast = 0) {
+                     int no_multicast = 0, void* splitk_ws = nullptr, size_t splitk_bytes = 0) {
   if (stats_done) *stats_done = false;
   if (m <= 0 || n <= 0) return cudaSuccess;
   cudaError_t e;
   trace_begin(kind, st);
   TcGemmArgs t{a,      lda,   a_mn,        b,   ldb,     b_mn, d, ldd, m, n, k, accumulate,
                raster_n_fastest, status, stats, stats_scale, d32, finalize, no_multicast};
+  t.splitk_ws = static_cast<float*>(splitk_ws);
+  t.splitk_ws_bytes = splitk_bytes;
   if (dtype == FLJSD_BF16 && tc_gemm_supported(t)) {
     e = launch_gemm_tc(t, st);
     if (stats_done) *stats_done = stats != nullptr;
@@ -290,10 +294,13 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
     // grad_input rows of this chunk = dZ . W_s (W_s stored [V x H]: B is N-major)
-    // (measured: sharing W through multicast does not pay for this one)
+    // (measured: sharing W through multicast does not pay for this one). A
+    // chunk with too few output tiles for the GPU splits the V contraction;
+    // the teacher logits are dead by now and hold the fp32 partials.
     e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_INPUT, zs, L.ld, 0, w_s, p->h_s, 1,
                  static_cast<char*>(grad_input) + (size_t)r0 * p->h_s * s, p->h_s, rows, p->h_s,
-                 p->v, 0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0, 1);
+                 p->v, 0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0, 1, zt,
+                 L.logits_bytes / 2);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
     // grad_weight (+)= dZ^T . X_s: both operands stored with the chunk rows as

@@ -238,6 +238,10 @@ struct KParams {
   int finalize;
   unsigned long long timeout_ns;  // limit of every mbarrier wait
   int stall_producer;             // test of the bounded waits: issue no copies
+  // split-K: unit t covers tile t / k_splits and k-blocks [s*kb_per, (s+1)*kb_per)
+  // of split s = t % k_splits, written as fp32 to partial[s][m][ldd]
+  int k_splits, kb_per_split;
+  float* partial;
   int* status;
 };
 
@@ -304,6 +308,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mb = MC ? 2 * mu + (int)rank : mu;
   };
+  auto unit_split = [&](int t, int& tile, int& split, int& kb0, int& kb1) {
+    if (p.k_splits > 1) {
+      tile = t / p.k_splits;
+      split = t - tile * p.k_splits;
+      kb0 = split * p.kb_per_split;
+      kb1 = min(p.num_k_blocks, kb0 + p.kb_per_split);
+    } else {
+      tile = t;
+      split = 0;
+      kb0 = 0;
+      kb1 = p.num_k_blocks;
+    }
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -315,10 +332,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int s = 0; s < STAGES; ++s) issued[s] = false;
       bool ok = !p.stall_producer;
       for (int t = unit0; ok && t < p.num_units; t += unit_step) {
-        int mb, nb;
-        tile_coords(t, mb, nb);
+        int mb, nb, tile, split, kb0, kb1;
+        unit_split(t, tile, split, kb0, kb1);
+        tile_coords(tile, mb, nb);
         const int m0 = mb * BM, n0 = nb * BN;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar(cb, smem_u32(&cb->empty[stage]), phase ^ 1u, p.status)) {
             ok = false;
             break;
@@ -377,7 +395,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!wait_bar(cb, smem_u32(&cb->tmem_empty[acc]), acc_phase ^ 1u, p.status)) break;
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + acc * ACC_COLS;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        int tile_i, split_i, kb0, kb1;
+        unit_split(t, tile_i, split_i, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar(cb, smem_u32(&cb->full[stage]), phase, p.status)) {
             ok = false;
             break;
@@ -396,7 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               bd = smem_desc(sb + kk * (UMMA_K * 128), 8192, 1024);
             else
               bd = smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
-            mma_bf16(tmem_d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16(tmem_d, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           // frees the stage once read (in both CTAs of a multicast pair)
           if (MC)
@@ -423,8 +443,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int sub = warp & 3;  // TMEM lane quarter this warp may access
     int local = 0;
     for (int t = unit0; t < p.num_units; t += unit_step, ++local) {
-      int mb, nb;
-      tile_coords(t, mb, nb);
+      int mb, nb, tile, split, kb0, kb1;
+      unit_split(t, tile, split, kb0, kb1);
+      tile_coords(tile, mb, nb);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       bool ok = true;
@@ -444,6 +465,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(tmem_base + ((uint32_t)(sub * 32) << 16) + acc * ACC_COLS + c * 32, v);
         if (!row_ok) continue;
         const int64_t col0 = (int64_t)nb * BN + c * 32;
+        if (p.k_splits > 1) {
+          // split-K partial: plain fp32 store, summed later in a fixed order
+          float* dst = p.partial + ((int64_t)split * p.m + row) * p.ldd + col0;
+          if (col0 + 32 <= p.n) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<float4*>(dst)[q] =
+                  make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          } else {
+            for (int e = 0; e < 32 && col0 + e < p.n; ++e) dst[e] = v[e];
+          }
+          continue;
+        }
         if (p.stats) {
           float cm = -INFINITY;
 #pragma unroll
@@ -594,6 +628,51 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// D[r, c] = round(sum over s of partial[s][r][c]), s in increasing order.
+__global__ void k_splitk_reduce(const float* __restrict__ part, int splits, int64_t m, int64_t n,
+                                int64_t ldd, __nv_bfloat16* __restrict__ D) {
+  const int64_t n8 = n / 8;
+  const int64_t total = m * n8;
+  const int64_t plane = m * ldd;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / n8, c = (i - r * n8) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < splits; ++s) {
+      const float4* src = reinterpret_cast<const float4*>(part + s * plane + r * ldd + c);
+      const float4 a = src[0], b = src[1];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    *reinterpret_cast<uint4*>(D + r * ldd + c) =
+        make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
+                   pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
+  }
+  // columns past the last multiple of 8
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < m * (n - n8 * 8);
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t w = n - n8 * 8;
+    const int64_t r = i / w, c = n8 * 8 + (i - r * w);
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) acc += part[s * plane + r * ldd + c];
+    D[r * ldd + c] = __float2bfloat16_rn(acc);
+  }
+}
+
+// Split-K factor for a contraction with too few output tiles to fill the GPU
+// (1 = no split); `ctas` is the number of CTAs to aim for.
+int splitk_factor(int64_t m, int64_t n, int64_t k, int ctas) {
+  const int64_t tiles = ((m + BM - 1) / BM) * ((n + BN - 1) / BN);
+  const int64_t kblocks = (k + BK - 1) / BK;
+  if (tiles * 2 > ctas || kblocks < 8) return 1;
+  int64_t s = ctas / tiles;
+  if (s > kblocks / 4) s = kblocks / 4;
+  if (s > 16) s = 16;
+  if (s < 2) return 1;
+  const int64_t per = (kblocks + s - 1) / s;
+  return (int)((kblocks + per - 1) / per);  // no empty split
+}
+
 // ---- host: tensor maps ------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -674,6 +753,13 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, __nv_bfloat16
 
 }  // namespace
 
+size_t tc_splitk_bytes(int64_t m, int64_t n, int64_t k, int ctas) {
+  const int s = splitk_factor(m, n, k, ctas);
+  if (s <= 1) return 0;
+  const int64_t ldd = (n + 7) / 8 * 8;
+  return (size_t)s * (size_t)m * (size_t)ldd * sizeof(float);
+}
+
 bool tc_gemm_supported(const TcGemmArgs& g) {
   auto al = [](const void* q) { return ((uintptr_t)q & 15u) == 0; };
   return g.m > 0 && g.n > 0 && g.k > 0 && al(g.a) && al(g.b) && al(g.d) && g.lda % 8 == 0 &&
@@ -741,6 +827,37 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.stats = g.stats;
   p.stats_scale = g.stats_scale;
   auto* d = reinterpret_cast<__nv_bfloat16*>(g.d);
+  // split-K when the output has too few tiles for the GPU (one-CTA schedule,
+  // plain stores only); the partials go to the caller's scratch.
+  // FLJSD_GEMM_SPLITK=0 in the environment turns it off.
+  p.k_splits = 1;
+  p.kb_per_split = p.num_k_blocks;
+  p.partial = nullptr;
+  const char* senv = getenv("FLJSD_GEMM_SPLITK");
+  const bool split_off = senv != nullptr && senv[0] == '0';
+  if (!mc && !split_off && g.splitk_ws != nullptr && !g.accumulate && g.d32 == nullptr &&
+      g.stats == nullptr) {
+    int s_ = splitk_factor(g.m, g.n, g.k, num_sms());
+    while (s_ > 1 && (size_t)s_ * (size_t)g.m * (size_t)g.ldd * sizeof(float) > g.splitk_ws_bytes)
+      --s_;
+    if (s_ > 1) {
+      p.kb_per_split = (p.num_k_blocks + s_ - 1) / s_;
+      p.k_splits = (p.num_k_blocks + p.kb_per_split - 1) / p.kb_per_split;
+      p.partial = g.splitk_ws;
+      p.num_units = p.num_tiles * p.k_splits;
+    }
+  }
+  if (p.k_splits > 1) {
+    cudaError_t e;
+    if (!g.a_mn && !g.b_mn) e = launch_t<false, false, false>(ma, mb, d, p, st);
+    else if (!g.a_mn && g.b_mn) e = launch_t<false, true, false>(ma, mb, d, p, st);
+    else if (g.a_mn && g.b_mn) e = launch_t<true, true, false>(ma, mb, d, p, st);
+    else e = launch_t<true, false, false>(ma, mb, d, p, st);
+    if (e != cudaSuccess) return e;
+    k_splitk_reduce<<<num_sms() * 4, 256, 0, st>>>(p.partial, p.k_splits, g.m, g.n, g.ldd, d);
+    count_extra_launch();
+    return cudaGetLastError();
+  }
   if (mc) {
     if (!g.a_mn && !g.b_mn) return launch_t<false, false, true>(ma, mb, d, p, st);
     if (!g.a_mn && g.b_mn) return launch_t<false, true, true>(ma, mb, d, p, st);

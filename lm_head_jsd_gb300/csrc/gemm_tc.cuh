@@ -40,9 +40,19 @@ struct TcGemmArgs {
   // kernel reports FLJSD_ERR_TIMEOUT in *status and exits cleanly.
   unsigned long long timeout_ns;
   int stall_producer;
+  // Optional fp32 scratch for split-K (used when the output has too few tiles
+  // to fill the GPU, accumulate == 0 and no d32 / stats): up to
+  // tc_splitk_bytes(m, n, k, ...) bytes, 16-byte aligned.
+  float* splitk_ws;
+  size_t splitk_ws_bytes;
 };
 
 constexpr int TC_TILE_N = 256;
+// CTAs a plan assumes when it sizes the split-K scratch (the launch uses the
+// device's own count, capped by the scratch it is given).
+constexpr int TC_PLAN_CTAS = 152;
+// Scratch bytes the split-K schedule of this contraction would use.
+size_t tc_splitk_bytes(int64_t m, int64_t n, int64_t k, int ctas);
 
 bool tc_gemm_supported(const TcGemmArgs& g);
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st);

@@ -15,6 +15,8 @@ namespace fljsd {
 // ---------------------------------------------------------------------------
 void trace_begin(int kind, cudaStream_t st);
 void trace_end(int kind, cudaStream_t st);
+// counts a kernel launched inside a traced call beyond the call's first
+void count_extra_launch();
 
 // Number of SMs of the current device (cached per device).
 int num_sms();

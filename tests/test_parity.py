@@ -309,3 +309,24 @@ def test_fp32_grad_weight_accumulation(chunk):
     out = run.forward(x_s, w_s, x_t, w_t, labels)
     torch.cuda.synchronize()
     compare(out, ref, "bf16", f"accum fp32 chunk={chunk}")
+
+
+@pytest.mark.parametrize("chunk", [128, 256])
+def test_split_k_grad_input(chunk, monkeypatch):
+    """A chunk with few output tiles splits the vocabulary contraction of
+    grad_input; the fp32 partials are summed in a fixed order and rounded
+    once. Loss and grad_weight do not depend on it (bitwise); grad_input
+    differs from the unsplit contraction only by fp32 summation order."""
+    w = jsd_inputs.custom("splitk", 41, 512, 512, 8192, "bf16", ignore_frac=0.1)
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    ref = _oracle(inputs, beta=0.5, temperature=1.0, reduction="batchmean")
+    split = run_gpu(*inputs, beta=0.5, reduction="batchmean", chunk_rows=chunk)
+    compare(split, ref, "bf16", f"split-K chunk={chunk}")
+    again = run_gpu(*inputs, beta=0.5, reduction="batchmean", chunk_rows=chunk)
+    for a, b in zip(split, again):
+        assert torch.equal(a, b), "split-K result is not reproducible"
+    monkeypatch.setenv("FLJSD_GEMM_SPLITK", "0")
+    whole = run_gpu(*inputs, beta=0.5, reduction="batchmean", chunk_rows=chunk)
+    compare(whole, ref, "bf16", f"unsplit chunk={chunk}")
+    assert torch.equal(split[0], whole[0]) and torch.equal(split[2], whole[2])
+    assert rel_fro(f64(split[1]), f64(whole[1])) <= 4e-3
