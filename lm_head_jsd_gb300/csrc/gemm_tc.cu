@@ -1,17 +1,27 @@
 // bf16 GEMM on the 5th-generation tensor cores (sm_103a): D (+)= A . B^T.
 //
 // Persistent, warp-specialised kernel, one CTA per SM:
-//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a 4-stage
-//               shared-memory ring (mbarrier complete_tx).
+//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a ring of
+//               up to 4 shared-memory stages (mbarrier complete_tx).
 //   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), tile
 //               128 x 256 x 16, accumulating in tensor memory; two 256-column
 //               accumulators so the epilogue of tile i overlaps the main loop
 //               of tile i+1. Warp 1 also allocates / frees the 512 TMEM columns.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, rounding to bf16 with
-//               16-byte stores, or a read-modify-write of the stored value (bf16
-//               or an fp32 side accumulator) for accumulation, and optionally
-//               the per-row (max, sum 2^(x - max)) partials of the stored tile
-//               (pass 1 of the online softmax).
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, rounding to bf16
+//               into shared-memory staging buffers written out by TMA stores
+//               (measured 2.3x the write rate of 16-byte stores per row and
+//               thread on a short-K contraction), or a read-modify-write of the
+//               stored value (bf16 or an fp32 side accumulator) for
+//               accumulation, and optionally the per-row (max, sum 2^(x - max))
+//               partials of the stored tile (pass 1 of the online softmax).
+//   warp 6      for an accumulating epilogue: TMA copies of the old output
+//               values, 128 rows x 128 bytes per slab, into a slab ring ahead
+//               of the epilogue, which adds the product in place and writes
+//               each slab back with one TMA store per warp. (A row-per-thread
+//               read-modify-write through plain loads keeps too few bytes in
+//               flight to reach HBM bandwidth.)
+// Contractions with too few output tiles for the GPU split K: fp32 partials
+// per split, summed in a fixed order by a second kernel.
 // Operands may be K-major (the contraction dimension contiguous) or MN-major;
 // the three contractions of the fused-linear JSD need: logits = X . W^T
 // (both K-major), grad_input = dZ . W (B MN-major), grad_weight = dZ^T . X
@@ -39,14 +49,27 @@ namespace fljsd {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
-constexpr int STAGES = 4;
+constexpr int STAGES = 4;  // operand stages (at most; see KParams::nst)
+constexpr int MAX_SLABS = 8;                    // prefetched slabs of the stored output
+constexpr int SLAB_BYTES = BM * 128;            // 128 rows x 128 bytes (64 bf16 / 32 fp32)
+constexpr int OUT_BUF_BYTES = 32 * 128;  // one warp's staging buffer: 32 rows x 128 B
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int ACC_COLS = BN;                    // fp32 accumulator columns per tile
 constexpr int TMEM_COLS = 2 * ACC_COLS;         // double-buffered accumulator
-constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int THREADS = 224;
+constexpr int SMEM_MAX = 232448;  // opt-in shared memory per CTA on sm_103
+// operand stages + slab ring + alignment slack + control block
+// nbuf: staging buffers per epilogue warp (0 without stage_out)
+__host__ __device__ constexpr int smem_bytes(int nst, int nslab, int nbuf) {
+  return nst * STAGE_BYTES + nslab * SLAB_BYTES + 4 * nbuf * OUT_BUF_BYTES + 1024 + 256;
+}
+static_assert(smem_bytes(2, 8, 0) <= SMEM_MAX && smem_bytes(3, 5, 0) <= SMEM_MAX &&
+                  smem_bytes(4, 2, 0) <= SMEM_MAX && smem_bytes(4, 2, 0) <= SMEM_MAX &&
+                  smem_bytes(4, 0, 2) <= SMEM_MAX && smem_bytes(3, 0, 4) <= SMEM_MAX &&
+                  smem_bytes(2, 0, 8) <= SMEM_MAX,
+              "shared memory");
 constexpr unsigned long long kTimeoutNs = 10ull * 1000 * 1000 * 1000;  // 10 s by default
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -84,6 +107,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 struct Ctrl {
   unsigned long long full[STAGES];
   unsigned long long empty[STAGES];
+  unsigned long long cfull[MAX_SLABS];   // slab of the stored output landed
+  unsigned long long cempty[MAX_SLABS];  // slab read by the four epilogue warps
   unsigned long long tmem_full[2];
   unsigned long long tmem_empty[2];
   unsigned long long drain;
@@ -130,6 +155,40 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* 
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
       : "memory");
 }
+// Shared -> global tensor copy (clipped at the tensor's bounds), tracked by
+// bulk groups of the issuing thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// all but the most recent bulk group have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// at most `keep` (1, 3 or 7) of the most recent bulk groups still read shared memory
+__device__ __forceinline__ void bulk_wait_read_keep(int keep) {
+  if (keep >= 7)
+    asm volatile("cp.async.bulk.wait_group.read 7;" ::: "memory");
+  else if (keep >= 3)
+    asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+  else
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// generic-proxy writes to shared memory become visible to later TMA reads
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -242,18 +301,34 @@ struct KParams {
   // of split s = t % k_splits, written as fp32 to partial[s][m][ldd]
   int k_splits, kb_per_split;
   float* partial;
+  // operand stages in use (<= STAGES), and the stored-output prefetch of an
+  // accumulating epilogue: warp 6 copies the old values of each tile with TMA
+  // into a ring of nslab slabs (slab_cols columns each, cps 32-column chunks
+  // per slab) ahead of the epilogue; nslab = 0 reads them with plain loads.
+  int nst, nslab, slab_cols, cps;
+  // slab_store: the new values go back into the slab and out with one TMA
+  // store per epilogue warp (its 32 rows); slab_f32: the slab holds fp32
+  int slab_store, slab_f32;
+  // stage_out (plain bf16 output, no slabs): each epilogue warp rounds its 32
+  // rows x 64 columns into one of nbuf (2, 4 or 8) shared-memory buffers and
+  // writes them with a TMA store (whole lines instead of 16 bytes per row and
+  // thread)
+  int stage_out, nbuf;
   int* status;
 };
 
 template <bool A_MN, bool B_MN, bool MC>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
               __nv_bfloat16* __restrict__ D, KParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  Ctrl* cb = reinterpret_cast<Ctrl*>(gbase + STAGES * STAGE_BYTES);
+  const uint32_t cslabs = base + p.nst * STAGE_BYTES;  // slab ring (1024-aligned)
+  uint8_t* stg = gbase + p.nst * STAGE_BYTES + p.nslab * SLAB_BYTES;  // output staging
+  Ctrl* cb = reinterpret_cast<Ctrl*>(stg + (p.stage_out ? 4 * p.nbuf * OUT_BUF_BYTES : 0));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -266,6 +341,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&cb->tmem_full[a]), 1);
       mbar_init(smem_u32(&cb->tmem_empty[a]), 4);
+    }
+    for (int s = 0; s < MAX_SLABS; ++s) {
+      mbar_init(smem_u32(&cb->cfull[s]), 1);
+      mbar_init(smem_u32(&cb->cempty[s]), 4);
     }
     mbar_init(smem_u32(&cb->drain), 1);
     cb->abort = 0;
@@ -370,7 +449,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           issued[stage] = true;
           issued_parity[stage] = phase;
-          if (++stage == STAGES) {
+          if (++stage == p.nst) {
             stage = 0;
             phase ^= 1u;
           }
@@ -424,7 +503,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           else
             mma_commit(smem_u32(&cb->empty[stage]));
           any = true;
-          if (++stage == STAGES) {
+          if (++stage == p.nst) {
             stage = 0;
             phase ^= 1u;
           }
@@ -438,10 +517,52 @@ __global__ void __launch_bounds__(THREADS, 1)
         wait_bar(cb, smem_u32(&cb->drain), 0, p.status);
       }
     }
+  } else if (warp == 6) {
+    // ---------------- stored-output prefetch ----------------
+    // The old values of each tile (bf16 D or the fp32 side accumulator), in
+    // slabs of 128 rows x 128 bytes, 128B-swizzled, in the epilogue's order.
+    if (lane == 0 && p.nslab > 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t issued_parity[MAX_SLABS];
+      bool issued[MAX_SLABS];
+      for (int s = 0; s < MAX_SLABS; ++s) issued[s] = false;
+      bool ok = true;
+      for (int t = unit0; ok && t < p.num_units; t += unit_step) {
+        int mb, nb, tile, split, kb0, kb1;
+        unit_split(t, tile, split, kb0, kb1);
+        tile_coords(tile, mb, nb);
+        const int n0 = nb * BN;
+        const int ncols = (int)min((int64_t)BN, p.n - n0);
+        const int nsl = (ncols + p.slab_cols - 1) / p.slab_cols;
+        for (int j = 0; j < nsl; ++j) {
+          if (!wait_bar(cb, smem_u32(&cb->cempty[slot]), phase ^ 1u, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&cb->cfull[slot]);
+          mbar_arrive_expect_tx(fb, SLAB_BYTES);
+          tma_load_2d(cslabs + slot * SLAB_BYTES, &tmC, fb, n0 + j * p.slab_cols, mb * BM);
+          issued[slot] = true;
+          issued_parity[slot] = phase;
+          if (++slot == p.nslab) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < MAX_SLABS; ++s)
+        if (issued[s]) wait_bar(cb, smem_u32(&cb->cfull[s]), issued_parity[s], p.status);
+    }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int sub = warp & 3;  // TMEM lane quarter this warp may access
     int local = 0;
+    int cslot = 0;  // slab ring position (same sequence as the prefetch warp)
+    uint32_t cphase = 0;
+    int pend = -1;  // slab whose TMA store may still be reading it (lane 0)
+    int sbuf = 0;   // staging buffer of this warp in use (stage_out)
+    bool dead = false;
     for (int t = unit0; t < p.num_units; t += unit_step, ++local) {
       int mb, nb, tile, split, kb0, kb1;
       unit_split(t, tile, split, kb0, kb1);
@@ -460,158 +581,280 @@ __global__ void __launch_bounds__(THREADS, 1)
       // the values as stored (rounded to bf16) times stats_scale: pass 1 of the
       // online softmax, done here while the tile is in registers
       float st_m = -INFINITY, st_d = 0.f;
+      const int nch = (int)((min((int64_t)BN, p.n - (int64_t)nb * BN) + 31) / 32);
       for (int c = 0; c < ACC_COLS / 32; ++c) {
+        if ((p.nslab > 0 || p.stage_out) && c >= nch) break;  // nothing to store, no slab
         float v[32];
         tmem_ld32(tmem_base + ((uint32_t)(sub * 32) << 16) + acc * ACC_COLS + c * 32, v);
-        if (!row_ok) continue;
-        const int64_t col0 = (int64_t)nb * BN + c * 32;
-        if (p.k_splits > 1) {
-          // split-K partial: plain fp32 store, summed later in a fixed order
-          float* dst = p.partial + ((int64_t)split * p.m + row) * p.ldd + col0;
-          if (col0 + 32 <= p.n) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              reinterpret_cast<float4*>(dst)[q] =
-                  make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-          } else {
-            for (int e = 0; e < 32 && col0 + e < p.n; ++e) dst[e] = v[e];
-          }
-          continue;
-        }
-        if (p.stats) {
-          float cm = -INFINITY;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float x = (col0 + e < p.n)
-                ? __fmul_rn(__bfloat162float(__float2bfloat16_rn(v[e])), p.stats_scale)
-                : -INFINITY;
-            cm = fmaxf(cm, x);
-          }
-          if (cm > st_m) {
-            st_d = (st_m == -INFINITY) ? 0.f : st_d * ex2f_approx(st_m - cm);
-            st_m = cm;
-          }
-          // exponent = x * scale - max with the exact product rounded once, so
-          // that large scaled logits (small T) keep their precision near the max
-          float acc_d = 0.f;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            if (col0 + e < p.n)
-              acc_d += ex2f_approx(
-                  __fmaf_rn(__bfloat162float(__float2bfloat16_rn(v[e])), p.stats_scale, -st_m));
-          }
-          st_d += acc_d;
-        }
-        // Read-modify-write of the stored value: issue the reads of the whole
-        // 32-column chunk before using any of them (they are independent).
-        const bool full_chunk = col0 + 32 <= p.n;
-        const bool rmw16 = p.accumulate && p.d32 == nullptr;
-        const bool rmw32 = p.d32 != nullptr && (p.accumulate || p.finalize);
-        if (full_chunk && (rmw16 || rmw32)) {
-          if (rmw16) {
-            const uint4* src = reinterpret_cast<const uint4*>(drow + col0);
-            uint4 o[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) o[q] = src[q];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t ow[4] = {o[q].x, o[q].y, o[q].z, o[q].w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                v[q * 8 + 2 * e] += bf16_lo(ow[e]);
-                v[q * 8 + 2 * e + 1] += bf16_hi(ow[e]);
-              }
+        uint8_t* crow = nullptr;  // this row's 128 bytes of the current slab
+        if (p.nslab > 0) {
+          if (c % p.cps == 0) {
+            const bool got = wait_bar(cb, smem_u32(&cb->cfull[cslot]), cphase, p.status);
+            if (!__all_sync(0xffffffffu, got)) {
+              dead = true;
+              break;
             }
-          } else {
-            const float4* src = reinterpret_cast<const float4*>(p.d32 + row * p.ldd + col0);
-            float4 o[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) o[q] = src[q];
+          }
+          crow = gbase + p.nst * STAGE_BYTES + cslot * SLAB_BYTES + (sub * 32 + lane) * 128;
+        }
+        if (p.stage_out && (c & 1) == 0) {
+          // the store that last used this staging buffer has read it
+          if (lane == 0) bulk_wait_read_keep(p.nbuf - 1);
+          __syncwarp();
+        }
+        if (p.slab_store) {
+          // old + product, written back in place (16-byte unit u of the
+          // swizzled row sits at u ^ (row & 7)); rows and columns past the
+          // output are zero-filled here and clipped by the store
+          if (p.slab_f32) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              v[4 * q] += o[q].x;
-              v[4 * q + 1] += o[q].y;
-              v[4 * q + 2] += o[q].z;
-              v[4 * q + 3] += o[q].w;
+              float4* u = reinterpret_cast<float4*>(crow + ((q ^ (lane & 7)) << 4));
+              const float4 o = *u;
+              *u = make_float4(o.x + v[4 * q], o.y + v[4 * q + 1], o.z + v[4 * q + 2],
+                               o.w + v[4 * q + 3]);
             }
-          }
-          if (p.d32 != nullptr && !p.finalize) {
-            float4* dst = reinterpret_cast<float4*>(p.d32 + row * p.ldd + col0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(drow + col0);
+            const int h = (c % p.cps) * 4;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(pack_bf16(v[q * 8], v[q * 8 + 1]), pack_bf16(v[q * 8 + 2], v[q * 8 + 3]),
-                                  pack_bf16(v[q * 8 + 4], v[q * 8 + 5]),
-                                  pack_bf16(v[q * 8 + 6], v[q * 8 + 7]));
-          }
-          continue;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int64_t col = col0 + q * 8;
-          if (col >= p.n) break;
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = v[q * 8 + e];
-          __nv_bfloat16* dst = drow + col;
-          if (p.d32 != nullptr) {
-            // fp32 accumulator: D32 (+)= product, or on the last pass
-            // D = round(D32 + product)
-            float* s32 = p.d32 + row * p.ldd + col;
-            const int ne = (col + 8 <= p.n) ? 8 : (int)(p.n - col);
-            if (ne == 8) {
-              if (p.accumulate || p.finalize) {
-                const float4 a0 = reinterpret_cast<const float4*>(s32)[0];
-                const float4 a1 = reinterpret_cast<const float4*>(s32)[1];
-                x[0] += a0.x; x[1] += a0.y; x[2] += a0.z; x[3] += a0.w;
-                x[4] += a1.x; x[5] += a1.y; x[6] += a1.z; x[7] += a1.w;
-              }
-              if (p.finalize) {
-                *reinterpret_cast<uint4*>(dst) =
-                    make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
-                               pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-              } else {
-                reinterpret_cast<float4*>(s32)[0] = make_float4(x[0], x[1], x[2], x[3]);
-                reinterpret_cast<float4*>(s32)[1] = make_float4(x[4], x[5], x[6], x[7]);
-              }
-            } else {
-              for (int e = 0; e < ne; ++e) {
-                float y = x[e];
-                if (p.accumulate || p.finalize) y += s32[e];
-                if (p.finalize) dst[e] = __float2bfloat16_rn(y);
-                else s32[e] = y;
-              }
-            }
-          } else if (col + 8 <= p.n) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
-            if (p.accumulate) {
-              const uint4 o = *d4;
+            for (int q = 0; q < 4; ++q) {
+              uint4* u = reinterpret_cast<uint4*>(crow + (((h + q) ^ (lane & 7)) << 4));
+              const uint4 o = *u;
               const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+              float x[8];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                x[2 * e] += bf16_lo(ow[e]);
-                x[2 * e + 1] += bf16_hi(ow[e]);
+                x[2 * e] = v[q * 8 + 2 * e] + bf16_lo(ow[e]);
+                x[2 * e + 1] = v[q * 8 + 2 * e + 1] + bf16_hi(ow[e]);
+              }
+              *u = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                              pack_bf16(x[6], x[7]));
+            }
+          }
+        } else do {  // `continue` ends this chunk's work; the slab is released below
+          if (!row_ok) continue;
+          const int64_t col0 = (int64_t)nb * BN + c * 32;
+          if (p.k_splits > 1) {
+            // split-K partial: plain fp32 store, summed later in a fixed order
+            float* dst = p.partial + ((int64_t)split * p.m + row) * p.ldd + col0;
+            if (col0 + 32 <= p.n) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(dst)[q] =
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+              for (int e = 0; e < 32 && col0 + e < p.n; ++e) dst[e] = v[e];
+            }
+            continue;
+          }
+          if (p.stats) {
+            float cm = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float x = (col0 + e < p.n)
+                  ? __fmul_rn(__bfloat162float(__float2bfloat16_rn(v[e])), p.stats_scale)
+                  : -INFINITY;
+              cm = fmaxf(cm, x);
+            }
+            if (cm > st_m) {
+              st_d = (st_m == -INFINITY) ? 0.f : st_d * ex2f_approx(st_m - cm);
+              st_m = cm;
+            }
+            // exponent = x * scale - max with the exact product rounded once, so
+            // that large scaled logits (small T) keep their precision near the max
+            float acc_d = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              if (col0 + e < p.n)
+                acc_d += ex2f_approx(
+                    __fmaf_rn(__bfloat162float(__float2bfloat16_rn(v[e])), p.stats_scale, -st_m));
+            }
+            st_d += acc_d;
+          }
+          if (p.stage_out) {
+            // rounded to bf16 into this warp's staging buffer (16-byte unit u
+            // of the swizzled 128-byte row sits at u ^ (row & 7))
+            uint8_t* srow = stg + ((sub * p.nbuf + sbuf) * 32 + lane) * 128;
+            const int h = (c & 1) * 4;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(srow + (((h + q) ^ (lane & 7)) << 4)) =
+                  make_uint4(pack_bf16(v[q * 8], v[q * 8 + 1]), pack_bf16(v[q * 8 + 2], v[q * 8 + 3]),
+                             pack_bf16(v[q * 8 + 4], v[q * 8 + 5]),
+                             pack_bf16(v[q * 8 + 6], v[q * 8 + 7]));
+            continue;
+          }
+          // Read-modify-write of the stored value: issue the reads of the whole
+          // 32-column chunk before using any of them (they are independent).
+          const bool full_chunk = col0 + 32 <= p.n;
+          const bool rmw16 = p.accumulate && p.d32 == nullptr;
+          const bool rmw32 = p.d32 != nullptr && (p.accumulate || p.finalize);
+          if (full_chunk && (rmw16 || rmw32)) {
+            if (rmw16) {
+              uint4 o[4];
+              if (crow != nullptr) {
+                // 16-byte units of the swizzled slab row: unit u sits at u ^ (row & 7)
+                const int h = (c % p.cps) * 4;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  o[q] = *reinterpret_cast<const uint4*>(crow + (((h + q) ^ (lane & 7)) << 4));
+              } else {
+                const uint4* src = reinterpret_cast<const uint4*>(drow + col0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) o[q] = src[q];
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t ow[4] = {o[q].x, o[q].y, o[q].z, o[q].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  v[q * 8 + 2 * e] += bf16_lo(ow[e]);
+                  v[q * 8 + 2 * e + 1] += bf16_hi(ow[e]);
+                }
+              }
+            } else {
+              float4 o[8];
+              if (crow != nullptr) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  o[q] = *reinterpret_cast<const float4*>(crow + ((q ^ (lane & 7)) << 4));
+              } else {
+                const float4* src = reinterpret_cast<const float4*>(p.d32 + row * p.ldd + col0);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) o[q] = src[q];
+              }
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                v[4 * q] += o[q].x;
+                v[4 * q + 1] += o[q].y;
+                v[4 * q + 2] += o[q].z;
+                v[4 * q + 3] += o[q].w;
               }
             }
-            *d4 = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
-                             pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-          } else {
-            for (int e = 0; e < 8 && col + e < p.n; ++e) {
-              float y = x[e];
-              if (p.accumulate) y += __bfloat162float(dst[e]);
-              dst[e] = __float2bfloat16_rn(y);
+            if (p.d32 != nullptr && !p.finalize) {
+              float4* dst = reinterpret_cast<float4*>(p.d32 + row * p.ldd + col0);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(drow + col0);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(pack_bf16(v[q * 8], v[q * 8 + 1]), pack_bf16(v[q * 8 + 2], v[q * 8 + 3]),
+                                    pack_bf16(v[q * 8 + 4], v[q * 8 + 5]),
+                                    pack_bf16(v[q * 8 + 6], v[q * 8 + 7]));
             }
+            continue;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t col = col0 + q * 8;
+            if (col >= p.n) break;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = v[q * 8 + e];
+            __nv_bfloat16* dst = drow + col;
+            if (p.d32 != nullptr) {
+              // fp32 accumulator: D32 (+)= product, or on the last pass
+              // D = round(D32 + product)
+              float* s32 = p.d32 + row * p.ldd + col;
+              const int ne = (col + 8 <= p.n) ? 8 : (int)(p.n - col);
+              if (ne == 8) {
+                if (p.accumulate || p.finalize) {
+                  const float4 a0 = reinterpret_cast<const float4*>(s32)[0];
+                  const float4 a1 = reinterpret_cast<const float4*>(s32)[1];
+                  x[0] += a0.x; x[1] += a0.y; x[2] += a0.z; x[3] += a0.w;
+                  x[4] += a1.x; x[5] += a1.y; x[6] += a1.z; x[7] += a1.w;
+                }
+                if (p.finalize) {
+                  *reinterpret_cast<uint4*>(dst) =
+                      make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                                 pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+                } else {
+                  reinterpret_cast<float4*>(s32)[0] = make_float4(x[0], x[1], x[2], x[3]);
+                  reinterpret_cast<float4*>(s32)[1] = make_float4(x[4], x[5], x[6], x[7]);
+                }
+              } else {
+                for (int e = 0; e < ne; ++e) {
+                  float y = x[e];
+                  if (p.accumulate || p.finalize) y += s32[e];
+                  if (p.finalize) dst[e] = __float2bfloat16_rn(y);
+                  else s32[e] = y;
+                }
+              }
+            } else if (col + 8 <= p.n) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+              if (p.accumulate) {
+                const uint4 o = *d4;
+                const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  x[2 * e] += bf16_lo(ow[e]);
+                  x[2 * e + 1] += bf16_hi(ow[e]);
+                }
+              }
+              *d4 = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                               pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+            } else {
+              for (int e = 0; e < 8 && col + e < p.n; ++e) {
+                float y = x[e];
+                if (p.accumulate) y += __bfloat162float(dst[e]);
+                dst[e] = __float2bfloat16_rn(y);
+              }
+            }
+          }
+        } while (0);
+        if (p.stage_out && ((c & 1) || c == nch - 1)) {
+          // 32 rows x 64 columns staged: one TMA store (clipped at the output's
+          // bounds)
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int64_t r0 = (int64_t)mb * BM + sub * 32;
+            if (r0 < p.m)
+              tma_store_2d(&tmS, smem_u32(stg + (sub * p.nbuf + sbuf) * OUT_BUF_BYTES),
+                           nb * BN + (c >> 1) * 64, (int32_t)r0);
+            bulk_commit();
+          }
+          if (++sbuf == p.nbuf) sbuf = 0;
+        }
+        if (p.nslab > 0 && ((c + 1) % p.cps == 0 || c == nch - 1)) {
+          // this warp is done with the slab
+          if (p.slab_store) {
+            // its 32 rows go out with one TMA store; the slab is handed back
+            // to the prefetch warp once the store has read it (one behind)
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int64_t r0 = (int64_t)mb * BM + sub * 32;
+              if (r0 < p.m)
+                tma_store_2d(&tmS, smem_u32(crow - lane * 128),
+                             nb * BN + (c / p.cps) * p.slab_cols, (int32_t)r0);
+              bulk_commit();
+              bulk_wait_read_1();
+              if (pend >= 0) mbar_arrive(smem_u32(&cb->cempty[pend]));
+            }
+            pend = cslot;
+          } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&cb->cempty[cslot]));
+          }
+          if (++cslot == p.nslab) {
+            cslot = 0;
+            cphase ^= 1u;
           }
         }
       }
+      if (dead) break;
       if (p.stats && row_ok) p.stats[row * p.num_n_blocks + nb] = make_float2(st_m, st_d);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&cb->tmem_empty[acc]));
+    }
+    if ((p.slab_store || p.stage_out) && lane == 0) {
+      // every store of this warp has completed before the CTA may exit
+      bulk_wait_all();
+      if (pend >= 0) mbar_arrive(smem_u32(&cb->cempty[pend]));
     }
   }
 
@@ -688,25 +931,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [outer x inner] matrix with row stride
-// ld elements; box = box_inner x box_outer; 128-byte swizzle; zero fill.
+// 2-D tensor map (bf16, or fp32 when f32) over a row-major [outer x inner]
+// matrix with row stride ld elements; box = box_inner x box_outer; 128-byte
+// swizzle; zero fill.
 bool make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
-              int box_inner, int box_outer) {
+              int box_inner, int box_outer, bool f32 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * (f32 ? 4 : 2)};
   cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 template <bool A_MN, bool B_MN, bool MC>
-cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, __nv_bfloat16* d, KParams p,
-                     cudaStream_t st) {
+cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mcm,
+                     const CUtensorMap& msm, __nv_bfloat16* d, KParams p, cudaStream_t st) {
+  const int smem = smem_bytes(p.nst, p.nslab, p.stage_out ? p.nbuf : 0);
   static int max_clusters[64] = {0};
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -715,13 +961,13 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, __nv_bfloat16
   auto kern = k_gemm_tc<A_MN, B_MN, MC>;
   if (!cache || !attr_set[dev]) {
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
     if (e != cudaSuccess) return e;
     if (cache) attr_set[dev] = true;
   }
   if (!MC) {
     const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
-    kern<<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, d, p);
+    kern<<<grid, THREADS, smem, st>>>(ma, mb, mcm, msm, d, p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -731,7 +977,7 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, __nv_bfloat16
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -746,7 +992,7 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, __nv_bfloat16
   const int mc = cache ? max_clusters[dev] : max_clusters[0];
   const int clusters = p.num_units < mc ? p.num_units : mc;
   cfg.gridDim = dim3(2 * clusters);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, d, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mcm, msm, d, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -847,27 +1093,82 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
       p.num_units = p.num_tiles * p.k_splits;
     }
   }
+  // stored-output prefetch for an accumulating epilogue (read-modify-write of
+  // D, or of the fp32 side accumulator): fewer operand stages, a slab ring for
+  // the old values. FLJSD_GEMM_PREFETCH=0 in the environment turns it off.
+  p.nst = STAGES;
+  p.nslab = 0;
+  p.slab_cols = 64;
+  p.cps = 2;
+  p.slab_store = 0;
+  p.slab_f32 = 0;
+  p.stage_out = 0;
+  p.nbuf = 0;
+  CUtensorMap mcm = ma, msm = ma;  // unused unless nslab > 0
+  const bool rmw = (g.accumulate && g.d32 == nullptr) ||
+                   (g.d32 != nullptr && (g.accumulate || g.finalize));
+  const char* penv = getenv("FLJSD_GEMM_PREFETCH");
+  const bool pf_off = penv != nullptr && penv[0] == '0';
+  if (rmw && p.k_splits == 1 && !pf_off) {
+    const bool f32 = g.d32 != nullptr;
+    const void* src = f32 ? (const void*)g.d32 : g.d;
+    if (((uintptr_t)src & 15u) == 0) {
+      p.slab_cols = f32 ? 32 : 64;
+      p.cps = p.slab_cols / 32;
+      // the new values go back through the slab unless they change type
+      // (fp32 accumulator in, bf16 result out) or the row length is not a
+      // whole number of 16-byte units (measured: the store then also writes
+      // the padding up to the next 16-byte boundary)
+      const bool store = !(f32 && g.finalize) && (g.n * (f32 ? 4 : 2)) % 16 == 0;
+      if (make_map(&mcm, src, g.n, g.m, g.ldd, p.slab_cols, BM, f32) &&
+          (!store || make_map(&msm, src, g.n, g.m, g.ldd, p.slab_cols, 32, f32))) {
+        p.slab_store = store ? 1 : 0;
+        p.slab_f32 = f32 ? 1 : 0;
+        // short contractions are bound by the read-modify-write: deeper ring
+        if (p.num_k_blocks <= 4) {
+          p.nst = 2;
+          p.nslab = 8;
+        } else if (p.num_k_blocks <= 16) {
+          p.nst = 3;
+          p.nslab = 5;
+        } else {
+          p.nst = 4;
+          p.nslab = 2;
+        }
+      }
+    }
+  }
+  // plain bf16 output through staging buffers and TMA stores (rows a whole
+  // number of 16-byte units: see the slab store above).
+  // FLJSD_GEMM_STAGE_OUT=0 in the environment turns it off.
+  const char* oenv = getenv("FLJSD_GEMM_STAGE_OUT");
+  const bool so_off = oenv != nullptr && oenv[0] == '0';
+  if (!rmw && !so_off && p.k_splits == 1 && g.d32 == nullptr && (g.n * 2) % 16 == 0 &&
+      make_map(&msm, g.d, g.n, g.m, g.ldd, 64, 32, false)) {
+    p.stage_out = 1;
+    p.nbuf = 2;  // measured: 4 or 8 buffers (with fewer operand stages) do not help
+  }
   if (p.k_splits > 1) {
     cudaError_t e;
-    if (!g.a_mn && !g.b_mn) e = launch_t<false, false, false>(ma, mb, d, p, st);
-    else if (!g.a_mn && g.b_mn) e = launch_t<false, true, false>(ma, mb, d, p, st);
-    else if (g.a_mn && g.b_mn) e = launch_t<true, true, false>(ma, mb, d, p, st);
-    else e = launch_t<true, false, false>(ma, mb, d, p, st);
+    if (!g.a_mn && !g.b_mn) e = launch_t<false, false, false>(ma, mb, mcm, msm, d, p, st);
+    else if (!g.a_mn && g.b_mn) e = launch_t<false, true, false>(ma, mb, mcm, msm, d, p, st);
+    else if (g.a_mn && g.b_mn) e = launch_t<true, true, false>(ma, mb, mcm, msm, d, p, st);
+    else e = launch_t<true, false, false>(ma, mb, mcm, msm, d, p, st);
     if (e != cudaSuccess) return e;
     k_splitk_reduce<<<num_sms() * 4, 256, 0, st>>>(p.partial, p.k_splits, g.m, g.n, g.ldd, d);
     count_extra_launch();
     return cudaGetLastError();
   }
   if (mc) {
-    if (!g.a_mn && !g.b_mn) return launch_t<false, false, true>(ma, mb, d, p, st);
-    if (!g.a_mn && g.b_mn) return launch_t<false, true, true>(ma, mb, d, p, st);
-    if (g.a_mn && g.b_mn) return launch_t<true, true, true>(ma, mb, d, p, st);
-    return launch_t<true, false, true>(ma, mb, d, p, st);
+    if (!g.a_mn && !g.b_mn) return launch_t<false, false, true>(ma, mb, mcm, msm, d, p, st);
+    if (!g.a_mn && g.b_mn) return launch_t<false, true, true>(ma, mb, mcm, msm, d, p, st);
+    if (g.a_mn && g.b_mn) return launch_t<true, true, true>(ma, mb, mcm, msm, d, p, st);
+    return launch_t<true, false, true>(ma, mb, mcm, msm, d, p, st);
   }
-  if (!g.a_mn && !g.b_mn) return launch_t<false, false, false>(ma, mb, d, p, st);
-  if (!g.a_mn && g.b_mn) return launch_t<false, true, false>(ma, mb, d, p, st);
-  if (g.a_mn && g.b_mn) return launch_t<true, true, false>(ma, mb, d, p, st);
-  return launch_t<true, false, false>(ma, mb, d, p, st);
+  if (!g.a_mn && !g.b_mn) return launch_t<false, false, false>(ma, mb, mcm, msm, d, p, st);
+  if (!g.a_mn && g.b_mn) return launch_t<false, true, false>(ma, mb, mcm, msm, d, p, st);
+  if (g.a_mn && g.b_mn) return launch_t<true, true, false>(ma, mb, mcm, msm, d, p, st);
+  return launch_t<true, false, false>(ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace fljsd

@@ -103,3 +103,70 @@ def test_gemm_pairs_and_single_ctas_agree_bitwise(a_mn, b_mn):
     fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d1, ldd, m, n, k, 0, None, 1)
     torch.cuda.synchronize()
     assert torch.equal(d0[:, :n], d1[:, :n])
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["pairs", "single"])
+@pytest.mark.parametrize("a_mn,b_mn", [(1, 1), (0, 0), (0, 1)])
+@pytest.mark.parametrize("shape", [(1000, 777, 128), (300, 1000, 640), (129, 4096, 2048),
+                                   (5000, 4096, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_gemm_accumulate_prefetch_matches_plain_loads(a_mn, b_mn, shape, flags, monkeypatch):
+    """The accumulating epilogue reads the old values from slabs copied ahead by
+    TMA (shallow, middle and deep operand rings by contraction length); with the
+    copy turned off it reads them with plain loads. Same arithmetic, so the
+    results agree bitwise; padding columns and rows past m stay untouched."""
+    from lm_head_jsd_gb300 import fljsd_gemm_bf16
+
+    m, n, k = shape
+    g = torch.Generator(device="cuda").manual_seed(m + n + k)
+    a, lda = _operand(a_mn, k if a_mn else m, m if a_mn else k, g)
+    b, ldb = _operand(b_mn, k if b_mn else n, n if b_mn else k, g)
+    ldd = -(-n // 8) * 8 + 8
+    base = torch.full((m + 2, ldd), 3.0, dtype=torch.bfloat16, device="cuda")
+    base[:m, :n] = torch.randn(m, n, generator=g, device="cuda").to(torch.bfloat16)
+    outs = []
+    for pf in ("1", "0"):
+        monkeypatch.setenv("FLJSD_GEMM_PREFETCH", pf)
+        buf = base.clone()
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, buf, ldd, m, n, k, 1, status, flags)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        assert torch.all(buf[:, n:] == 3.0) and torch.all(buf[m:] == 3.0)
+        outs.append(buf)
+    assert torch.equal(outs[0], outs[1])
+    ref = base[:m, :n].float() + _ref(a, a_mn, b, b_mn)
+    err = (outs[0][:m, :n].float() - ref).norm() / ref.norm()
+    assert err < 4e-3, float(err)
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["pairs", "single"])
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("shape", [(1000, 1000, 128), (129, 4096, 640), (300, 264, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_gemm_staged_output_matches_plain_stores(a_mn, b_mn, shape, flags, monkeypatch):
+    """A plain (non-accumulating) bf16 output goes through shared-memory staging
+    buffers and TMA stores; with staging turned off each thread stores its row.
+    Same rounding, so the results agree bitwise; the stores are clipped at the
+    output's bounds (padding columns and rows past m untouched)."""
+    from lm_head_jsd_gb300 import fljsd_gemm_bf16
+
+    m, n, k = shape
+    g = torch.Generator(device="cuda").manual_seed(m * 3 + n + k)
+    a, lda = _operand(a_mn, k if a_mn else m, m if a_mn else k, g)
+    b, ldb = _operand(b_mn, k if b_mn else n, n if b_mn else k, g)
+    ldd = n + 16
+    outs = []
+    for so in ("1", "0"):
+        monkeypatch.setenv("FLJSD_GEMM_STAGE_OUT", so)
+        buf = torch.full((m + 2, ldd), 5.0, dtype=torch.bfloat16, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, buf, ldd, m, n, k, 0, status, flags)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        assert torch.all(buf[:, n:] == 5.0) and torch.all(buf[m:] == 5.0)
+        outs.append(buf)
+    assert torch.equal(outs[0], outs[1])
+    ref = _ref(a, a_mn, b, b_mn)
+    err = (outs[0][:m, :n].float() - ref).norm() / ref.norm()
+    assert err < 4e-3, float(err)

@@ -295,7 +295,7 @@ def test_t2_scaling_flag(dt, beta):
 
 
 @pytest.mark.parametrize("chunk", [1, 7, 64])
-def test_fp32_grad_weight_accumulation(chunk):
+def test_fp32_grad_weight_accumulation(chunk, monkeypatch):
     """With the fp32 accumulator, hundreds of chunks stay within the bf16
     tolerance (without it, 300 one-row chunks drift to ~1.8e-2)."""
     from lm_head_jsd_gb300 import FusedLinearJSD
@@ -306,9 +306,16 @@ def test_fp32_grad_weight_accumulation(chunk):
     x_s, w_s, x_t, w_t, labels = (t.cuda() for t in inputs)
     run = FusedLinearJSD(300, 64, 64, 5000, torch.bfloat16, chunk_rows=chunk, accum_fp32=True)
     assert run.plan.workspace_bytes >= 5000 * 64 * 4
-    out = run.forward(x_s, w_s, x_t, w_t, labels)
+    out = [t.clone() for t in run.forward(x_s, w_s, x_t, w_t, labels)]
     torch.cuda.synchronize()
     compare(out, ref, "bf16", f"accum fp32 chunk={chunk}")
+    # the accumulator read through TMA-prefetched slabs or through plain loads:
+    # same arithmetic, same bits
+    monkeypatch.setenv("FLJSD_GEMM_PREFETCH", "0")
+    plain = run.forward(x_s, w_s, x_t, w_t, labels)
+    torch.cuda.synchronize()
+    for a, b in zip(out, plain):
+        assert torch.equal(a, b)
 
 
 @pytest.mark.parametrize("chunk", [128, 256])
