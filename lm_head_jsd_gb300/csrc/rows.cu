@@ -58,37 +58,59 @@ __device__ __forceinline__ void md_fold(MD& s, const float (&z)[N], float c) {
   s.d += acc;
 }
 
-// Block-wide reductions in a fixed order (deterministic).
-__device__ __forceinline__ MD block_md(MD v, MD* sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Block-wide reductions in a fixed order (deterministic): a butterfly inside
+// each warp, the per-warp results through shared memory, a butterfly over
+// them in warp 0, and the total broadcast from slot NW. sh holds NW + 1.
+__device__ __forceinline__ MD warp_md(MD v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     MD u{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.d, o)};
     v = md_combine(v, u);
   }
+  return v;
+}
+template <int NW>
+__device__ __forceinline__ MD block_md(MD v, MD* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_md(v);
   if (lane == 0) sh[warp] = v;
   __syncthreads();
-  MD r = sh[0];
-  for (int w = 1; w < kWarps; ++w) r = md_combine(r, sh[w]);
+  if (warp == 0) {
+    MD u = lane < NW ? sh[lane] : MD{-CUDART_INF_F, 0.f};
+    u = warp_md(u);
+    if (lane == 0) sh[NW] = u;
+  }
   __syncthreads();
-  return r;
+  return sh[NW];
 }
 
-__device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ __forceinline__ float2 warp_sum2(float2 v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
     v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
   }
+  return v;
+}
+template <int NW>
+__device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum2(v);
   if (lane == 0) sh[warp] = v;
   __syncthreads();
-  float2 r = sh[0];
-  for (int w = 1; w < kWarps; ++w) {
-    r.x += sh[w].x;
-    r.y += sh[w].y;
+  if (warp == 0) {
+    float2 u = lane < NW ? sh[lane] : make_float2(0.f, 0.f);
+    u = warp_sum2(u);
+    if (lane == 0) sh[NW] = u;
   }
   __syncthreads();
+  return sh[NW];
+}
+
+// Two floats to fp16x2 (lo in the low half), saturated to the finite range.
+__device__ __forceinline__ uint32_t pack_half2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
@@ -113,8 +135,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
   using V = Vec<T>;
   constexpr bool PREC = sizeof(T) == 4;
   constexpr int N = V::N;
-  __shared__ MD sh_md[kWarps];
-  __shared__ float2 sh_s[kWarps];
+  __shared__ MD sh_md[kWarps + 1];
+  __shared__ float2 sh_s[kWarps + 1];
   extern __shared__ uint4 xm_cache[];  // lean path: fp16 X - log M of cache_vec vectors
 
   const float c = a.scale_log2;  // log2(e) / T
@@ -175,8 +197,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
         md_fold<1>(mb, xt, c);
       }
     }
-    const MD ra = block_md(ma, sh_md);
-    const MD rb = block_md(mb, sh_md);
+    const MD ra = block_md<kWarps>(ma, sh_md);
+    const MD rb = block_md<kWarps>(mb, sh_md);
     // log2 Q_j = z_j * c - m_a - log2 d_a, formed as fma(z, c, -m) - log2 d so
     // that the exact product is rounded once relative to the row maximum.
     // A one-element row has log-prob 0 whatever its logit.
@@ -211,15 +233,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
           xm8[k] = xm;
         }
         if (v < ncache) {
-          uint32_t h[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            // clamped into the fp16 range: where |xm| is that large Q is 0
-            __half2 t = __floats2half2_rn(fminf(fmaxf(xm8[2 * e], -6.0e4f), 6.0e4f),
-                                          fminf(fmaxf(xm8[2 * e + 1], -6.0e4f), 6.0e4f));
-            h[e] = *reinterpret_cast<uint32_t*>(&t);
-          }
-          cache[v] = make_uint4(h[0], h[1], h[2], h[3]);
+          // saturated to the fp16 range: where |xm| is that large Q is 0
+          cache[v] = make_uint4(pack_half2_sat(xm8[0], xm8[1]), pack_half2_sat(xm8[2], xm8[3]),
+                                pack_half2_sat(xm8[4], xm8[5]), pack_half2_sat(xm8[6], xm8[7]));
         }
       };
       int64_t i = threadIdx.x;
@@ -245,7 +261,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
         accq = fmaf(Q, xm, accq);
         accp = fmaf(P, ym, accp);
       }
-      const float2 tot = block_sum2(make_float2(accq, accp), sh_s);  // also orders the cache
+      const float2 tot = block_sum2<kWarps>(make_float2(accq, accp), sh_s);  // also orders the cache
       const float S2 = omb * tot.x;
       const float L2 = fmaf(beta, tot.y, S2);
       if (threadIdx.x == 0) a.loss_rows[grow] = 0.6931471805599453f * L2 * a.loss_scale;
@@ -319,7 +335,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       acc.x += ell;
       acc.y += g;
     }
-    const float2 tot = block_sum2(acc, sh_s);
+    const float2 tot = block_sum2<kWarps>(acc, sh_s);
     const float L2 = tot.x, S2 = tot.y;  // row loss and dX_sum, / ln 2
     if (threadIdx.x == 0) a.loss_rows[grow] = 0.6931471805599453f * L2 * a.loss_scale;
 
