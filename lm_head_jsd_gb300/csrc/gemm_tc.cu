@@ -189,6 +189,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -350,6 +354,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     cb->abort = 0;
     cb->timeout_ns = p.timeout_ns;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // bring the tensor maps into the TMA unit's descriptor cache up front
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if (p.nslab > 0) prefetch_tensormap(&tmC);
+    if (p.slab_store || p.stage_out) prefetch_tensormap(&tmS);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
