@@ -46,16 +46,31 @@ def _peaks():
                 "source": "fallback"}
 
 
-def _profiled_traffic(kernel: str, source: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when the kernel's source has changed since the counters were taken."""
-    import glob
+GEMM_SOURCES = ("gemm_tc.cuh", "gemm_tc_kernel.cuh", "gemm_tc.cu", "gemm_tc_kk.cu",
+                "gemm_tc_kmn.cu", "gemm_tc_mnmn.cu", "gemm_tc_mnk.cu")
+ROWS_SOURCES = ("rows.cu",)
+
+
+def sources_hash(sources) -> str | None:
+    """First 16 hex digits of the SHA-256 of the named kernel sources, in order."""
     import hashlib
 
-    src = os.path.join(ROOT, "lm_head_jsd_gb300", "csrc", source)
+    h = hashlib.sha256()
     try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for name in sources:
+            h.update(open(os.path.join(ROOT, "lm_head_jsd_gb300", "csrc", name), "rb").read())
     except OSError:
+        return None
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(kernel: str, sources):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the kernel's sources have changed since the counters were taken."""
+    import glob
+
+    h = sources_hash(sources)
+    if h is None:
         return None
     for path in glob.glob(os.path.join(ROOT, "profiles", "dram_traffic_*.md")):
         vals = {}
@@ -333,7 +348,7 @@ def main():
         "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (4 launches per chunk)",
                      "achieved": round(achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tc, 4),
-                     "traffic": _profiled_traffic("k_gemm_tc", "gemm_tc.cu")
+                     "traffic": _profiled_traffic("k_gemm_tc", GEMM_SOURCES)
                      if w.name == "headline" else None,
                      "peak_kind": f"bf16 sustained ({peaks['source']})"},
         "roofline_step": {"flop": flop_step, "roofline_ms": round(step_roof_ms, 3),
@@ -343,7 +358,7 @@ def main():
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(jsd_gbs / peaks["hbm_gbs"], 4),
                          "algorithmic_bytes": "3*C*V*s per launch",
-                         "traffic": _profiled_traffic("k_jsd_rows", "rows.cu")
+                         "traffic": _profiled_traffic("k_jsd_rows", ROWS_SOURCES)
                          if w.name == "headline" else None},
         "kernel_ms_per_step": {k: round(v[0] / max(steps_traced, 1), 4) for k, v in kinds.items()},
         "gpu_launches": launches,

@@ -40,7 +40,9 @@ def nvcc() -> str:
 
 
 def sources() -> list[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    # the kernel instantiation units take longest: start them first
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(srcs, key=lambda s: not os.path.basename(s).startswith("gemm_tc_"))
 
 
 def _deps() -> list[str]:

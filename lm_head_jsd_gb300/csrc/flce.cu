@@ -220,7 +220,7 @@ struct CeLayout {
 CeLayout ce_layout(const fljsd_ce_problem& p, int64_t c) {
   CeLayout L{};
   L.ld = (p.v + 7) / 8 * 8;
-  L.ntiles = (p.v + TC_TILE_N - 1) / TC_TILE_N;
+  L.ntiles = (p.v + TC_STATS_COLS - 1) / TC_STATS_COLS;
   const size_t zb = align_up((size_t)c * (size_t)L.ld * dsize(p.dtype));
   const size_t sb = align_up((size_t)c * (size_t)L.ntiles * sizeof(float2));
   L.z = 0;

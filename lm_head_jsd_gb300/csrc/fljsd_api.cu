@@ -93,8 +93,8 @@ Layout layout_for(const fljsd_problem& p, int64_t chunk_rows) {
   L.ld = (p.v + 7) / 8 * 8;
   const size_t s = dtype_size(p.dtype);
   const size_t zbytes = align_up((size_t)chunk_rows * (size_t)L.ld * s);
-  // per-row, per-256-column-tile pass-1 partials written by the logits GEMMs
-  L.ntiles = (p.v + TC_TILE_N - 1) / TC_TILE_N;
+  // per-row pass-1 partials of every 128 columns, written by the logits GEMMs
+  L.ntiles = (p.v + TC_STATS_COLS - 1) / TC_STATS_COLS;
   const size_t sbytes = align_up((size_t)chunk_rows * (size_t)L.ntiles * sizeof(float2));
   L.zs = 0;
   L.zt = zbytes;

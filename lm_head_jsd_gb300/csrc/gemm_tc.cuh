@@ -24,7 +24,8 @@ struct TcGemmArgs {
   int raster_n_fastest;
   int* status;           // device word that receives FLJSD_ERR_TIMEOUT, or null
   // Optional row statistics of the stored output (requires accumulate == 0):
-  // for row r and n-tile j (TC_TILE_N columns), stats[r * ceil(n / TC_TILE_N) + j]
+  // for row r and column block j (TC_STATS_COLS columns),
+  // stats[r * ceil(n / TC_STATS_COLS) + j]
   // = (m, sum 2^(x - m)) over x = bf16(D[r, col]) * stats_scale, where m is the
   // largest rounded product and each x - m is formed from the exact product.
   float2* stats;
@@ -47,7 +48,7 @@ struct TcGemmArgs {
   size_t splitk_ws_bytes;
 };
 
-constexpr int TC_TILE_N = 256;
+constexpr int TC_STATS_COLS = 128;  // columns per pass-1 partial
 // CTAs a plan assumes when it sizes the split-K scratch (the launch uses the
 // device's own count, capped by the scratch it is given).
 constexpr int TC_PLAN_CTAS = 152;

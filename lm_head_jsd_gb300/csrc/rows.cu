@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
     // ---- pass 1: m/d of student (a) and teacher (b) together ----
     MD ma{-CUDART_INF_F, 0.f}, mb{-CUDART_INF_F, 0.f};
     if (a.stats_s != nullptr) {
-      // the logits GEMM already folded each 256-column tile of this row
+      // the logits GEMM already folded each 128 columns of this row
       const float2* ps = a.stats_s + r * a.ntiles;
       const float2* pt = a.stats_t + r * a.ntiles;
       for (int64_t i = threadIdx.x; i < a.ntiles; i += blockDim.x) {

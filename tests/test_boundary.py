@@ -59,8 +59,8 @@ def test_plan_single_chunk_and_memory_accounting(L):
     assert plan.logits_bytes == 2 * 8192 * 128256 * 2
     assert plan.workspace_bytes >= plan.logits_bytes + 8192 * 4
     # beyond the logits: loss_1d (BT*4), the pass-1 partials of both models
-    # (8 bytes per row per 256-column tile each) and alignment
-    partials = 2 * 8192 * (-(-128256 // 256)) * 8
+    # (8 bytes per row per 128 columns each) and alignment
+    partials = 2 * 8192 * (-(-128256 // 128)) * 8
     assert plan.stats_bytes >= partials + 8192 * 4
     extra = plan.workspace_bytes - plan.logits_bytes
     assert partials + 8192 * 4 <= extra < partials + 8192 * 4 + 4096
