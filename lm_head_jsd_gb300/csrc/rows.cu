@@ -124,7 +124,9 @@ __device__ __forceinline__ void lean_terms(float zs, float zt, float c, float oa
   const float Y2 = __fmaf_rn(zt, c, -ob);
   Q = ex2(X2);
   P = ex2(Y2);
-  const float lM = lg2(fmaxf(fmaf(omb, Q, beta * P), 1.17549435e-38f));
+  // M + 2^-126 instead of max(M, 2^-126): the same guard against log2(0)
+  // where both terms flush to zero, one instruction less
+  const float lM = lg2(fmaf(omb, Q, fmaf(beta, P, 1.17549435e-38f)));
   const bool tie = X2 == Y2;
   xm = tie ? 0.f : X2 - lM;
   ym = tie ? 0.f : Y2 - lM;
@@ -219,10 +221,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
     if (BRANCH == 2 && !PREC && fabsf(ma_) < 64.f && fabsf(mb_) < 64.f) {
       const float oa = ma_ + lda, ob = mb_ + ldb;
       float accq = 0.f, accp = 0.f;
-      const int64_t step = blockDim.x;
-      const int64_t ncache = nvec < a.cache_vec ? nvec : a.cache_vec;
+      // 32-bit vector indices (nvec < 2^27): less index arithmetic per vector
+      const int step = (int)blockDim.x;
+      const int nv = (int)nvec;
+      const int ncache = (int)(nvec < a.cache_vec ? nvec : a.cache_vec);
       uint4* cache = reinterpret_cast<uint4*>(xm_cache);
-      auto pass2_vec = [&](const float (&xs)[N], const float (&xt)[N], int64_t v) {
+      auto pass2_vec = [&](const float (&xs)[N], const float (&xt)[N], int v) {
         float xm8[N];
 #pragma unroll
         for (int k = 0; k < N; ++k) {
@@ -238,9 +242,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
                                 pack_half2_sat(xm8[4], xm8[5]), pack_half2_sat(xm8[6], xm8[7]));
         }
       };
-      int64_t i = threadIdx.x;
+      int i = (int)threadIdx.x;
       // two vectors per iteration: four 16-byte loads in flight per thread
-      for (; i + step < nvec; i += 2 * step) {
+      for (; i + step < nv; i += 2 * step) {
         float xs[N], xt[N], xs2[N], xt2[N];
         V::load(zs + i * N, xs);
         V::load(zt + i * N, xt);
@@ -249,7 +253,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
         pass2_vec(xs, xt, i);
         pass2_vec(xs2, xt2, i + step);
       }
-      for (; i < nvec; i += step) {
+      for (; i < nv; i += step) {
         float xs[N], xt[N];
         V::load(zs + i * N, xs);
         V::load(zt + i * N, xt);
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       // dz = ln2 * scale * Q * ((1-beta) xm - S)
       const float k0 = 0.6931471805599453f * w * a.inv_temperature * a.loss_scale;
       const float k1 = k0 * omb, k2 = k0 * S2;
-      auto pass3_vec = [&](int64_t v) {
+      auto pass3_vec = [&](int v) {
         float xs[N];
         V::load(zs + v * N, xs);
         if (v < ncache) {
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       };
       // walk the row backwards: the lines pass 2 read last are the likeliest
       // to still be in L2
-      int64_t i3 = nvec - 1 - threadIdx.x;
+      int i3 = nv - 1 - (int)threadIdx.x;
       for (; i3 - step >= 0; i3 -= 2 * step) {
         pass3_vec(i3);
         pass3_vec(i3 - step);
