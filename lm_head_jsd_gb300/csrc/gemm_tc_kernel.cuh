@@ -336,6 +336,136 @@ struct KParams {
   int* status;
 };
 
+// The remaining ways of storing one 32-column chunk of a row: read-modify-write
+// through global memory (bf16 D or the fp32 side accumulator, or from a slab
+// that is not written back), plain 16-byte stores per row and thread, and the
+// ragged right edge. Kept out of line so that the epilogue loop's common paths
+// (staging for TMA stores, the slab read-modify-write) stay compact in the
+// instruction cache, which the other warps' loops share.
+static __device__ __noinline__ void store_chunk_generic(const KParams& p, float* v, int64_t row,
+                                                        int64_t col0, __nv_bfloat16* drow,
+                                                        const uint8_t* crow, int c, int lane) {
+  // Read-modify-write of the stored value: issue the reads of the whole
+  // 32-column chunk before using any of them (they are independent).
+  const bool full_chunk = col0 + 32 <= p.n;
+  const bool rmw16 = p.accumulate && p.d32 == nullptr;
+  const bool rmw32 = p.d32 != nullptr && (p.accumulate || p.finalize);
+  if (full_chunk && (rmw16 || rmw32)) {
+    if (rmw16) {
+      uint4 o[4];
+      if (crow != nullptr) {
+        // 16-byte units of the swizzled slab row: unit u sits at u ^ (row & 7)
+        const int h = (c % p.cps) * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          o[q] = *reinterpret_cast<const uint4*>(crow + (((h + q) ^ (lane & 7)) << 4));
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(drow + col0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = src[q];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t ow[4] = {o[q].x, o[q].y, o[q].z, o[q].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[q * 8 + 2 * e] += bf16_lo(ow[e]);
+          v[q * 8 + 2 * e + 1] += bf16_hi(ow[e]);
+        }
+      }
+    } else {
+      float4 o[8];
+      if (crow != nullptr) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          o[q] = *reinterpret_cast<const float4*>(crow + ((q ^ (lane & 7)) << 4));
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(p.d32 + row * p.ldd + col0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) o[q] = src[q];
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v[4 * q] += o[q].x;
+        v[4 * q + 1] += o[q].y;
+        v[4 * q + 2] += o[q].z;
+        v[4 * q + 3] += o[q].w;
+      }
+    }
+    if (p.d32 != nullptr && !p.finalize) {
+      float4* dst = reinterpret_cast<float4*>(p.d32 + row * p.ldd + col0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(drow + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_uint4(pack_bf16(v[q * 8], v[q * 8 + 1]), pack_bf16(v[q * 8 + 2], v[q * 8 + 3]),
+                            pack_bf16(v[q * 8 + 4], v[q * 8 + 5]),
+                            pack_bf16(v[q * 8 + 6], v[q * 8 + 7]));
+    }
+    return;
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int64_t col = col0 + q * 8;
+    if (col >= p.n) break;
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = v[q * 8 + e];
+    __nv_bfloat16* dst = drow + col;
+    if (p.d32 != nullptr) {
+      // fp32 accumulator: D32 (+)= product, or on the last pass
+      // D = round(D32 + product)
+      float* s32 = p.d32 + row * p.ldd + col;
+      const int ne = (col + 8 <= p.n) ? 8 : (int)(p.n - col);
+      if (ne == 8) {
+        if (p.accumulate || p.finalize) {
+          const float4 a0 = reinterpret_cast<const float4*>(s32)[0];
+          const float4 a1 = reinterpret_cast<const float4*>(s32)[1];
+          x[0] += a0.x; x[1] += a0.y; x[2] += a0.z; x[3] += a0.w;
+          x[4] += a1.x; x[5] += a1.y; x[6] += a1.z; x[7] += a1.w;
+        }
+        if (p.finalize) {
+          *reinterpret_cast<uint4*>(dst) =
+              make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                         pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+        } else {
+          reinterpret_cast<float4*>(s32)[0] = make_float4(x[0], x[1], x[2], x[3]);
+          reinterpret_cast<float4*>(s32)[1] = make_float4(x[4], x[5], x[6], x[7]);
+        }
+      } else {
+        for (int e = 0; e < ne; ++e) {
+          float y = x[e];
+          if (p.accumulate || p.finalize) y += s32[e];
+          if (p.finalize) dst[e] = __float2bfloat16_rn(y);
+          else s32[e] = y;
+        }
+      }
+    } else if (col + 8 <= p.n) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      if (p.accumulate) {
+        const uint4 o = *d4;
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          x[2 * e] += bf16_lo(ow[e]);
+          x[2 * e + 1] += bf16_hi(ow[e]);
+        }
+      }
+      *d4 = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                       pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+    } else {
+      for (int e = 0; e < 8 && col + e < p.n; ++e) {
+        float y = x[e];
+        if (p.accumulate) y += __bfloat162float(dst[e]);
+        dst[e] = __float2bfloat16_rn(y);
+      }
+    }
+  }
+}
+
 template <bool A_MN, bool B_MN, bool MC, int G>
 __global__ void __launch_bounds__(threads_for(G), 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -727,124 +857,11 @@ __global__ void __launch_bounds__(threads_for(G), 1)
                              pack_bf16(v[q * 8 + 6], v[q * 8 + 7]));
             continue;
           }
-          // Read-modify-write of the stored value: issue the reads of the whole
-          // 32-column chunk before using any of them (they are independent).
-          const bool full_chunk = col0 + 32 <= p.n;
-          const bool rmw16 = p.accumulate && p.d32 == nullptr;
-          const bool rmw32 = p.d32 != nullptr && (p.accumulate || p.finalize);
-          if (full_chunk && (rmw16 || rmw32)) {
-            if (rmw16) {
-              uint4 o[4];
-              if (crow != nullptr) {
-                // 16-byte units of the swizzled slab row: unit u sits at u ^ (row & 7)
-                const int h = (c % p.cps) * 4;
+          {
+            float vv[32];  // the out-of-line path takes the values through memory
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  o[q] = *reinterpret_cast<const uint4*>(crow + (((h + q) ^ (lane & 7)) << 4));
-              } else {
-                const uint4* src = reinterpret_cast<const uint4*>(drow + col0);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) o[q] = src[q];
-              }
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint32_t ow[4] = {o[q].x, o[q].y, o[q].z, o[q].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  v[q * 8 + 2 * e] += bf16_lo(ow[e]);
-                  v[q * 8 + 2 * e + 1] += bf16_hi(ow[e]);
-                }
-              }
-            } else {
-              float4 o[8];
-              if (crow != nullptr) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                  o[q] = *reinterpret_cast<const float4*>(crow + ((q ^ (lane & 7)) << 4));
-              } else {
-                const float4* src = reinterpret_cast<const float4*>(p.d32 + row * p.ldd + col0);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) o[q] = src[q];
-              }
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                v[4 * q] += o[q].x;
-                v[4 * q + 1] += o[q].y;
-                v[4 * q + 2] += o[q].z;
-                v[4 * q + 3] += o[q].w;
-              }
-            }
-            if (p.d32 != nullptr && !p.finalize) {
-              float4* dst = reinterpret_cast<float4*>(p.d32 + row * p.ldd + col0);
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(drow + col0);
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(pack_bf16(v[q * 8], v[q * 8 + 1]), pack_bf16(v[q * 8 + 2], v[q * 8 + 3]),
-                                    pack_bf16(v[q * 8 + 4], v[q * 8 + 5]),
-                                    pack_bf16(v[q * 8 + 6], v[q * 8 + 7]));
-            }
-            continue;
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int64_t col = col0 + q * 8;
-            if (col >= p.n) break;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = v[q * 8 + e];
-            __nv_bfloat16* dst = drow + col;
-            if (p.d32 != nullptr) {
-              // fp32 accumulator: D32 (+)= product, or on the last pass
-              // D = round(D32 + product)
-              float* s32 = p.d32 + row * p.ldd + col;
-              const int ne = (col + 8 <= p.n) ? 8 : (int)(p.n - col);
-              if (ne == 8) {
-                if (p.accumulate || p.finalize) {
-                  const float4 a0 = reinterpret_cast<const float4*>(s32)[0];
-                  const float4 a1 = reinterpret_cast<const float4*>(s32)[1];
-                  x[0] += a0.x; x[1] += a0.y; x[2] += a0.z; x[3] += a0.w;
-                  x[4] += a1.x; x[5] += a1.y; x[6] += a1.z; x[7] += a1.w;
-                }
-                if (p.finalize) {
-                  *reinterpret_cast<uint4*>(dst) =
-                      make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
-                                 pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-                } else {
-                  reinterpret_cast<float4*>(s32)[0] = make_float4(x[0], x[1], x[2], x[3]);
-                  reinterpret_cast<float4*>(s32)[1] = make_float4(x[4], x[5], x[6], x[7]);
-                }
-              } else {
-                for (int e = 0; e < ne; ++e) {
-                  float y = x[e];
-                  if (p.accumulate || p.finalize) y += s32[e];
-                  if (p.finalize) dst[e] = __float2bfloat16_rn(y);
-                  else s32[e] = y;
-                }
-              }
-            } else if (col + 8 <= p.n) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst);
-              if (p.accumulate) {
-                const uint4 o = *d4;
-                const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  x[2 * e] += bf16_lo(ow[e]);
-                  x[2 * e + 1] += bf16_hi(ow[e]);
-                }
-              }
-              *d4 = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
-                               pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-            } else {
-              for (int e = 0; e < 8 && col + e < p.n; ++e) {
-                float y = x[e];
-                if (p.accumulate) y += __bfloat162float(dst[e]);
-                dst[e] = __float2bfloat16_rn(y);
-              }
-            }
+            for (int e = 0; e < 32; ++e) vv[e] = v[e];
+            store_chunk_generic(p, vv, row, col0, drow, crow, c, lane);
           }
         } while (0);
         if (p.stage_out && ((c & 1) || c == nch - 1)) {
