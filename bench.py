@@ -48,7 +48,7 @@ def _peaks():
 
 GEMM_SOURCES = ("gemm_tc.cuh", "gemm_tc_kernel.cuh", "gemm_tc.cu", "gemm_tc_kk.cu",
                 "gemm_tc_kmn.cu", "gemm_tc_mnmn.cu", "gemm_tc_mnk.cu")
-ROWS_SOURCES = ("rows.cu",)
+ROWS_SOURCES = ("rows.cu", "jsd_math.cuh")
 
 
 def sources_hash(sources) -> str | None:
