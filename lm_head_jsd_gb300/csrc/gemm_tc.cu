@@ -269,6 +269,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
     p.epi_groups = 2;
     if (p.stage_out) p.nst = 3;  // room for 8 warps x 2 staging buffers
   }
+  p.epi_mode = p.stage_out ? EPI_STAGE
+                           : (p.slab_store && !p.slab_f32 ? EPI_SLAB16 : EPI_GENERIC);
   if (p.k_splits > 1) {
     cudaError_t e = launch_layout(g.a_mn, g.b_mn, false, ma, mb, mcm, msm, d, p, st);
     if (e != cudaSuccess) return e;

@@ -69,6 +69,8 @@ constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int ACC_COLS = BN;                    // fp32 accumulator columns per tile
 constexpr int TMEM_COLS = 2 * ACC_COLS;         // double-buffered accumulator
+constexpr int EPI_STAGE = 0, EPI_SLAB16 = 1, EPI_GENERIC = 2;
+
 // 7 warps (roles at the kernel), 11 with the second epilogue group
 __host__ __device__ constexpr int threads_for(int groups) { return groups == 2 ? 352 : 224; }
 constexpr int SMEM_MAX = 232448;  // opt-in shared memory per CTA on sm_103
@@ -332,6 +334,12 @@ struct KParams {
   // epilogue warps: one group of four (warps 2-5: all 256 columns of a tile),
   // or two (warps 7-10 take columns 128-255) where the epilogue is the bound
   int epi_groups;
+  // epilogue mode, also the kernel's template parameter (so that the common
+  // paths carry no runtime branches on it): EPI_STAGE staging + TMA stores
+  // (plain bf16 output, optional pass-1 partials), EPI_SLAB16 bf16 slab
+  // read-modify-write, EPI_GENERIC everything else (split-K partials, the fp32
+  // side accumulator, plain or read-modify-write stores from registers)
+  int epi_mode;
   int stat_tiles;  // pass-1 partials per row: one per 128 columns
   int* status;
 };
@@ -466,7 +474,7 @@ static __device__ __noinline__ void store_chunk_generic(const KParams& p, float*
   }
 }
 
-template <bool A_MN, bool B_MN, bool MC, int G>
+template <bool A_MN, bool B_MN, bool MC, int G, int EPI>
 __global__ void __launch_bounds__(threads_for(G), 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
@@ -721,6 +729,10 @@ __global__ void __launch_bounds__(threads_for(G), 1)
     // all earlier tiles of this CTA come first (the prefetch warp's order)
     int tslot = 0;
     uint32_t tphase = 0;
+    // the mode's paths, fixed at compile time where the mode fixes them
+    constexpr bool kStage = EPI == EPI_STAGE;
+    const bool kSlabStore = EPI == EPI_SLAB16 || (EPI == EPI_GENERIC && p.slab_store);
+    const bool kSlabs = EPI == EPI_SLAB16 || (EPI == EPI_GENERIC && p.nslab > 0);
     int pend = -1;  // slab whose TMA store may still be reading it (lane 0)
     int sbuf = 0;   // staging buffer of this warp in use (stage_out)
     bool dead = false;
@@ -754,7 +766,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
         float v[32];
         tmem_ld32(tmem_base + ((uint32_t)(sub * 32) << 16) + acc * ACC_COLS + c * 32, v);
         uint8_t* crow = nullptr;  // this row's 128 bytes of the current slab
-        if (p.nslab > 0) {
+        if (kSlabs) {
           cslot = tslot + (p.cps == 2 ? c >> 1 : c);
           uint32_t cphase = tphase;
           while (cslot >= p.nslab) {
@@ -770,16 +782,16 @@ __global__ void __launch_bounds__(threads_for(G), 1)
           }
           crow = gbase + p.nst * STAGE_BYTES + cslot * SLAB_BYTES + (sub * 32 + lane) * 128;
         }
-        if (p.stage_out && (c & 1) == 0) {
+        if (kStage && (c & 1) == 0) {
           // the store that last used this staging buffer has read it
           if (lane == 0) bulk_wait_read_keep(p.nbuf - 1);
           __syncwarp();
         }
-        if (p.slab_store) {
+        if (kSlabStore) {
           // old + product, written back in place (16-byte unit u of the
           // swizzled row sits at u ^ (row & 7)); rows and columns past the
           // output are zero-filled here and clipped by the store
-          if (p.slab_f32) {
+          if (EPI == EPI_GENERIC) {  // the fp32 side accumulator
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               float4* u = reinterpret_cast<float4*>(crow + ((q ^ (lane & 7)) << 4));
@@ -807,7 +819,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
         } else do {  // `continue` ends this chunk's work; the slab is released below
           if (!row_ok) continue;
           const int64_t col0 = (int64_t)nb * BN + c * 32;
-          if (p.k_splits > 1) {
+          if (EPI == EPI_GENERIC && p.k_splits > 1) {
             // split-K partial: plain fp32 store, summed later in a fixed order
             float* dst = p.partial + ((int64_t)split * p.m + row) * p.ldd + col0;
             if (col0 + 32 <= p.n) {
@@ -844,7 +856,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
             }
             st_d += acc_d;
           }
-          if (p.stage_out) {
+          if (kStage) {
             // rounded to bf16 into this warp's staging buffer (16-byte unit u
             // of the swizzled 128-byte row sits at u ^ (row & 7))
             uint8_t* srow = stg + ((ew * p.nbuf + sbuf) * 32 + lane) * 128;
@@ -857,14 +869,14 @@ __global__ void __launch_bounds__(threads_for(G), 1)
                              pack_bf16(v[q * 8 + 6], v[q * 8 + 7]));
             continue;
           }
-          {
+          if constexpr (EPI == EPI_GENERIC) {
             float vv[32];  // the out-of-line path takes the values through memory
 #pragma unroll
             for (int e = 0; e < 32; ++e) vv[e] = v[e];
             store_chunk_generic(p, vv, row, col0, drow, crow, c, lane);
           }
         } while (0);
-        if (p.stage_out && ((c & 1) || c == nch - 1)) {
+        if (kStage && ((c & 1) || c == nch - 1)) {
           // 32 rows x 64 columns staged: one TMA store (clipped at the output's
           // bounds)
           fence_proxy_async_smem();
@@ -878,9 +890,9 @@ __global__ void __launch_bounds__(threads_for(G), 1)
           }
           if (++sbuf == p.nbuf) sbuf = 0;
         }
-        if (p.nslab > 0 && ((c + 1) % p.cps == 0 || c == nch - 1)) {
+        if (kSlabs && ((c + 1) % p.cps == 0 || c == nch - 1)) {
           // this warp is done with the slab
-          if (p.slab_store) {
+          if (kSlabStore) {
             // its 32 rows go out with one TMA store; the slab is handed back
             // to the prefetch warp once the store has read it (one behind)
             fence_proxy_async_smem();
@@ -908,7 +920,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
         }
       }
       if (dead) break;
-      if (p.nslab > 0) {
+      if (kSlabs) {
         tslot += (ncols + p.slab_cols - 1) / p.slab_cols;
         while (tslot >= p.nslab) {
           tslot -= p.nslab;
@@ -919,7 +931,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&cb->tmem_empty[acc]));
     }
-    if ((p.slab_store || p.stage_out) && lane == 0) {
+    if ((kSlabStore || kStage) && lane == 0) {
       // every store of this warp has completed before the CTA may exit
       bulk_wait_all();
       if (pend >= 0) mbar_arrive(smem_u32(&cb->cempty[pend]));
@@ -939,7 +951,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
   }
 }
 
-template <bool A_MN, bool B_MN, bool MC, int G>
+template <bool A_MN, bool B_MN, bool MC, int G, int EPI>
 cudaError_t launch_g(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mcm,
                      const CUtensorMap& msm, __nv_bfloat16* d, KParams p, cudaStream_t st) {
   constexpr int THREADS = threads_for(G);
@@ -949,7 +961,7 @@ cudaError_t launch_g(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
   int dev = 0;
   cudaGetDevice(&dev);
   const bool cache = dev >= 0 && dev < 64;
-  auto kern = k_gemm_tc<A_MN, B_MN, MC, G>;
+  auto kern = k_gemm_tc<A_MN, B_MN, MC, G, EPI>;
   if (!cache || !attr_set[dev]) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
@@ -986,6 +998,21 @@ cudaError_t launch_g(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mcm, msm, d, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Every (epilogue groups, epilogue mode) variant of one layout and schedule.
+template <bool A_MN, bool B_MN, bool MC>
+cudaError_t launch_modes(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mcm,
+                         const CUtensorMap& msm, __nv_bfloat16* d, const KParams& p,
+                         cudaStream_t st) {
+  if (p.epi_groups == 2) {
+    if (p.epi_mode == EPI_STAGE) return launch_g<A_MN, B_MN, MC, 2, EPI_STAGE>(ma, mb, mcm, msm, d, p, st);
+    if (p.epi_mode == EPI_SLAB16) return launch_g<A_MN, B_MN, MC, 2, EPI_SLAB16>(ma, mb, mcm, msm, d, p, st);
+    return launch_g<A_MN, B_MN, MC, 2, EPI_GENERIC>(ma, mb, mcm, msm, d, p, st);
+  }
+  if (p.epi_mode == EPI_STAGE) return launch_g<A_MN, B_MN, MC, 1, EPI_STAGE>(ma, mb, mcm, msm, d, p, st);
+  if (p.epi_mode == EPI_SLAB16) return launch_g<A_MN, B_MN, MC, 1, EPI_SLAB16>(ma, mb, mcm, msm, d, p, st);
+  return launch_g<A_MN, B_MN, MC, 1, EPI_GENERIC>(ma, mb, mcm, msm, d, p, st);
 }
 
 // Launchers of one operand layout (A K-major or MN-major, B likewise), each

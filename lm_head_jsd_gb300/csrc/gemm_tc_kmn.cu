@@ -5,11 +5,8 @@ namespace fljsd {
 namespace tcgemm {
 
 FLJSD_TC_LAUNCHER(launch_kmn) {
-  if (mc)
-    return p.epi_groups == 2 ? launch_g<false, true, true, 2>(ma, mb, mcm, msm, d, p, st)
-                             : launch_g<false, true, true, 1>(ma, mb, mcm, msm, d, p, st);
-  return p.epi_groups == 2 ? launch_g<false, true, false, 2>(ma, mb, mcm, msm, d, p, st)
-                           : launch_g<false, true, false, 1>(ma, mb, mcm, msm, d, p, st);
+  return mc ? launch_modes<false, true, true>(ma, mb, mcm, msm, d, p, st)
+            : launch_modes<false, true, false>(ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace tcgemm

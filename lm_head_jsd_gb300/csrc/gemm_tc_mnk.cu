@@ -5,11 +5,8 @@ namespace fljsd {
 namespace tcgemm {
 
 FLJSD_TC_LAUNCHER(launch_mnk) {
-  if (mc)
-    return p.epi_groups == 2 ? launch_g<true, false, true, 2>(ma, mb, mcm, msm, d, p, st)
-                             : launch_g<true, false, true, 1>(ma, mb, mcm, msm, d, p, st);
-  return p.epi_groups == 2 ? launch_g<true, false, false, 2>(ma, mb, mcm, msm, d, p, st)
-                           : launch_g<true, false, false, 1>(ma, mb, mcm, msm, d, p, st);
+  return mc ? launch_modes<true, false, true>(ma, mb, mcm, msm, d, p, st)
+            : launch_modes<true, false, false>(ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace tcgemm
