@@ -228,9 +228,11 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
         p.slab_store = store ? 1 : 0;
         p.slab_f32 = f32 ? 1 : 0;
         // short contractions are bound by the read-modify-write: deeper ring
-        // (measured on 128256 x 4096 outputs: K = 128 and 512 fastest with two
-        // stages, eight slabs and two epilogue groups, K = 1024 with 3 / 5 / one)
-        if (p.num_k_blocks <= 8) {
+        // (measured on 128256 x 4096 outputs: up to K = 256 fastest with two
+        // stages, eight slabs and two epilogue groups (K = 128: 320 us against
+        // 431 us with 3 / 5 / one group), K = 512 and 1024 with 3 / 5 / one
+        // (K = 512: 514 us against 673 us), beyond that 4 / 2 / one)
+        if (p.num_k_blocks <= 4) {
           p.nst = 2;
           p.nslab = 8;
         } else if (p.num_k_blocks <= 16) {
@@ -260,12 +262,11 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   // needs 8 entries: with one release deferred per warp, two groups can hold
   // back up to 5 entries of the fp32 ring (3 of the bf16 one). Measured on
   // 128256 x 4096 outputs (same box, against one group): read-modify-write
-  // 735 -> 471 us at K = 128 and 750 -> 657 us at K = 512; write-only
-  // 369 -> 291 us at K = 128, but 404 -> 437 us at K = 512, where the fourth
-  // operand stage that the second group's staging buffers displace matters
-  // more.
+  // 431 -> 320 us at K = 128; write-only 233 -> 190 us at K = 128, even at
+  // K = 192, but 244 -> 301 us at K = 256, where the fourth operand stage
+  // that the second group's staging buffers displace matters more.
   p.epi_groups = 1;
-  if ((p.nslab == 8 && p.kb_per_split <= 8) || (p.nslab == 0 && p.kb_per_split <= 4)) {
+  if ((p.nslab == 8 && p.kb_per_split <= 4) || (p.nslab == 0 && p.kb_per_split <= 3)) {
     p.epi_groups = 2;
     if (p.stage_out) p.nst = 3;  // room for 8 warps x 2 staging buffers
   }
