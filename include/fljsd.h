@@ -216,7 +216,8 @@ fljsd_status fljsd_workspace_status(const fljsd_plan_t* plan, const void* worksp
  *   D stored [m x ldd]. All bf16, device, 16-byte aligned; lda, ldb, ldd
  *   multiples of 8; m, n, k >= 1.
  * status: device int32 that receives FLJSD_ERR_TIMEOUT if a bounded wait
- * expires (may be NULL). flags: 0 or FLJSD_GEMM_NO_MULTICAST (below).
+ * expires (may be NULL). flags: 0, FLJSD_GEMM_SINGLE_CTA or
+ * FLJSD_GEMM_TEST_STALL (below).
  * Asynchronous on `stream`. FLJSD_ERR_INVALID_ARG for
  * shapes or alignments outside the above.
  */
@@ -224,12 +225,10 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
                              int64_t ldb, int32_t b_mn, void* d, int64_t ldd, int64_t m,
                              int64_t n, int64_t k, int32_t accumulate, int32_t* status,
                              int32_t flags, fljsd_stream_t stream);
-/* flags of fljsd_gemm_bf16: by default pairs of 128-row blocks of D run as
- * 2-CTA clusters that fetch each B tile once for both (TMA multicast);
- * FLJSD_GEMM_NO_MULTICAST runs one CTA per tile. The results are identical.
- * The environment variable FLJSD_GEMM_MULTICAST=0 selects one CTA per tile for
- * every GEMM of the library (read at each launch). */
-#define FLJSD_GEMM_NO_MULTICAST 1
+/* flags of fljsd_gemm_bf16: FLJSD_GEMM_SINGLE_CTA runs every 128 x 256 tile of
+ * D on one CTA, which is the only schedule of this build (the flag is accepted
+ * and changes nothing). */
+#define FLJSD_GEMM_SINGLE_CTA 1
 /* Test of the failure path: the kernel's copy warp issues nothing, so its
  * first bounded wait expires after 50 ms; *status then holds
  * FLJSD_ERR_TIMEOUT, D is not written, and the context stays usable. */

@@ -201,7 +201,7 @@ def fljsd_workspace_status(plan, workspace, stream=None) -> int:
     return out.value
 
 
-FLJSD_GEMM_NO_MULTICAST = 1
+FLJSD_GEMM_SINGLE_CTA = 1
 FLJSD_GEMM_TEST_STALL = 2
 
 

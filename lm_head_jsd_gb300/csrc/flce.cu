@@ -260,14 +260,14 @@ cudaError_t ce_gemm(int dtype, int kind, const void* a, int64_t lda, int a_mn, c
                     int64_t ldb, int b_mn, void* d, int64_t ldd, int64_t m, int64_t n, int64_t k,
                     int accumulate, int raster_n_fastest, int* status, cudaStream_t st,
                     float2* stats, float stats_scale, bool* stats_done, float* d32,
-                    int finalize, int no_multicast = 0, void* splitk_ws = nullptr,
+                    int finalize, void* splitk_ws = nullptr,
                     size_t splitk_bytes = 0) {
   if (stats_done) *stats_done = false;
   if (m <= 0 || n <= 0) return cudaSuccess;
   cudaError_t e;
   trace_begin(kind, st);
   TcGemmArgs t{a,      lda,   a_mn,        b,   ldb,     b_mn, d, ldd, m, n, k, accumulate,
-               raster_n_fastest, status, stats, stats_scale, d32, finalize, no_multicast};
+               raster_n_fastest, status, stats, stats_scale, d32, finalize};
   t.splitk_ws = static_cast<float*>(splitk_ws);
   t.splitk_ws_bytes = splitk_bytes;
   if (dtype == FLJSD_BF16 && tc_gemm_supported(t)) {
@@ -385,7 +385,7 @@ fljsd_status fljsd_ce_forward(const fljsd_ce_problem* p, const fljsd_plan_t* pla
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
     e = ce_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_INPUT, z, L.ld, 0, w, p->h, 1,
                 static_cast<char*>(grad_input) + (size_t)r0 * p->h * s, p->h, rows, p->h, p->v,
-                0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0, 1, ws + L.splitk,
+                0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0, ws + L.splitk,
                 L.splitk_bytes);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
     const bool last = r0 + rows >= p->bt;

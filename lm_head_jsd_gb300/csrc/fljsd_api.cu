@@ -142,13 +142,13 @@ cudaError_t run_gemm(int dtype, int kind, const void* a, int64_t lda, int a_mn, 
                      int accumulate, int raster_n_fastest, int* status, cudaStream_t st,
                      float2* stats = nullptr, float stats_scale = 0.f,
                      bool* stats_done = nullptr, float* d32 = nullptr, int finalize = 0,
-                     int no_multicast = 0, void* splitk_ws = nullptr, size_t splitk_bytes = 0) {
+                     void* splitk_ws = nullptr, size_t splitk_bytes = 0) {
   if (stats_done) *stats_done = false;
   if (m <= 0 || n <= 0) return cudaSuccess;
   cudaError_t e;
   trace_begin(kind, st);
   TcGemmArgs t{a,      lda,   a_mn,        b,   ldb,     b_mn, d, ldd, m, n, k, accumulate,
-               raster_n_fastest, status, stats, stats_scale, d32, finalize, no_multicast};
+               raster_n_fastest, status, stats, stats_scale, d32, finalize};
   t.splitk_ws = static_cast<float*>(splitk_ws);
   t.splitk_ws_bytes = splitk_bytes;
   if (dtype == FLJSD_BF16 && tc_gemm_supported(t)) {
@@ -196,11 +196,17 @@ fljsd_status fljsd_plan(const fljsd_problem* p, size_t free_hbm_bytes, fljsd_pla
     c = p->bt;
   } else {
     const size_t budget = free_hbm_bytes / 2;
-    const Layout one = layout_for(*p, 1);
-    const Layout zero = layout_for(*p, 0);
-    const size_t per_row = one.total - zero.total;  // upper bound per row (alignment included)
-    if (budget < one.total) return FLJSD_ERR_WORKSPACE;
-    int64_t fit = (int64_t)((budget - zero.total) / (per_row > 0 ? per_row : 1));
+    // One chunk first: it needs no fp32 grad_weight accumulator, which the
+    // estimate below charges to every multi-chunk plan.
+    int64_t fit = p->bt;
+    if (layout_for(*p, p->bt).total > budget) {
+      const Layout one = layout_for(*p, 1);
+      const Layout zero = layout_for(*p, 0);
+      const size_t per_row = one.total - zero.total;  // upper bound per row (alignment included)
+      if (budget < one.total) return FLJSD_ERR_WORKSPACE;
+      fit = (int64_t)((budget - zero.total) / (per_row > 0 ? per_row : 1));
+      if (fit >= p->bt) fit = p->bt - 1;  // the one-chunk plan did not fit
+    }
     if (fit >= p->bt) {
       c = p->bt;
     } else {
@@ -293,13 +299,12 @@ fljsd_status fljsd_forward(const fljsd_problem* p, const fljsd_plan_t* plan, con
     e = launch_jsd_rows(p->dtype, ra, stream);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
-    // grad_input rows of this chunk = dZ . W_s (W_s stored [V x H]: B is N-major)
-    // (measured: sharing W through multicast does not pay for this one). A
-    // chunk with too few output tiles for the GPU splits the V contraction;
+    // grad_input rows of this chunk = dZ . W_s (W_s stored [V x H]: B is N-major).
+    // A chunk with too few output tiles for the GPU splits the V contraction;
     // the teacher logits are dead by now and hold the fp32 partials.
     e = run_gemm(p->dtype, FLJSD_KERNEL_GEMM_GRAD_INPUT, zs, L.ld, 0, w_s, p->h_s, 1,
                  static_cast<char*>(grad_input) + (size_t)r0 * p->h_s * s, p->h_s, rows, p->h_s,
-                 p->v, 0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0, 1, zt,
+                 p->v, 0, 1, status, stream, nullptr, 0.f, nullptr, nullptr, 0, zt,
                  L.logits_bytes / 2);
     if (e != cudaSuccess) return FLJSD_ERR_CUDA;
 
@@ -358,7 +363,7 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
                              int64_t ldb, int32_t b_mn, void* d, int64_t ldd, int64_t m,
                              int64_t n, int64_t k, int32_t accumulate, int32_t* status,
                              int32_t flags, fljsd_stream_t stream_) {
-  if ((flags & ~(FLJSD_GEMM_NO_MULTICAST | FLJSD_GEMM_TEST_STALL)) != 0)
+  if ((flags & ~(FLJSD_GEMM_SINGLE_CTA | FLJSD_GEMM_TEST_STALL)) != 0)
     return FLJSD_ERR_INVALID_ARG;
   if (!a || !b || !d || m <= 0 || n <= 0 || k <= 0) return FLJSD_ERR_INVALID_ARG;
   if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1) || (accumulate != 0 && accumulate != 1))
@@ -366,8 +371,7 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
   if (lda < (a_mn ? m : k) || ldb < (b_mn ? n : k) || ldd < n) return FLJSD_ERR_INVALID_ARG;
   const bool stall = (flags & FLJSD_GEMM_TEST_STALL) != 0;
   TcGemmArgs t{a,       lda,  a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, 1, status,
-               nullptr, 0.f,  nullptr, 0, (flags & FLJSD_GEMM_NO_MULTICAST) ? 1 : 0,
-               stall ? 50ull * 1000 * 1000 : 0ull, stall ? 1 : 0};
+               nullptr, 0.f,  nullptr, 0, stall ? 50ull * 1000 * 1000 : 0ull, stall ? 1 : 0};
   if (!tc_gemm_supported(t)) return FLJSD_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   trace_begin(FLJSD_KERNEL_SMALL, stream);

@@ -1,6 +1,6 @@
 // Tensor-core GEMM, host side: operand tensor maps, the schedule choice
-// (2-CTA pairs, tile order, split-K, stored-output prefetch, staging, epilogue
-// groups) and the split-K reduction. The kernel and its design notes are in
+// (tile order, split-K, stored-output prefetch, staging, epilogue groups) and
+// the split-K reduction. The kernel and its design notes are in
 // gemm_tc_kernel.cuh.
 #include "gemm_tc_kernel.cuh"
 
@@ -91,13 +91,13 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int
 }
 
 // One launch in the layout of (a_mn, b_mn).
-cudaError_t launch_layout(bool a_mn, bool b_mn, bool mc, const CUtensorMap& ma,
-                          const CUtensorMap& mb, const CUtensorMap& mcm, const CUtensorMap& msm,
-                          __nv_bfloat16* d, const KParams& p, cudaStream_t st) {
-  if (!a_mn && !b_mn) return launch_kk(ma, mb, mcm, msm, d, p, mc, st);
-  if (!a_mn && b_mn) return launch_kmn(ma, mb, mcm, msm, d, p, mc, st);
-  if (a_mn && b_mn) return launch_mnmn(ma, mb, mcm, msm, d, p, mc, st);
-  return launch_mnk(ma, mb, mcm, msm, d, p, mc, st);
+cudaError_t launch_layout(bool a_mn, bool b_mn, const CUtensorMap& ma, const CUtensorMap& mb,
+                          const CUtensorMap& mcm, const CUtensorMap& msm, __nv_bfloat16* d,
+                          const KParams& p, cudaStream_t st) {
+  if (!a_mn && !b_mn) return launch_kk(ma, mb, mcm, msm, d, p, st);
+  if (!a_mn && b_mn) return launch_kmn(ma, mb, mcm, msm, d, p, st);
+  if (a_mn && b_mn) return launch_mnmn(ma, mb, mcm, msm, d, p, st);
+  return launch_mnk(ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace
@@ -118,14 +118,7 @@ bool tc_gemm_supported(const TcGemmArgs& g) {
 
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   if (!tc_gemm_supported(g)) return cudaErrorInvalidValue;
-  // pairs of m-blocks share B through a 2-CTA cluster whenever there are two
-  // m-blocks to pair (and g.no_multicast is not set)
   const int64_t mblocks = (g.m + BM - 1) / BM;
-  // FLJSD_GEMM_MULTICAST=0 in the environment selects one CTA per tile for
-  // every call (both schedules compute identical results)
-  const char* env = getenv("FLJSD_GEMM_MULTICAST");
-  const bool env_off = env != nullptr && env[0] == '0';
-  const bool mc = mblocks >= 2 && !g.no_multicast && !env_off;
   CUtensorMap ma, mb;
   bool ok;
   if (g.a_mn)  // A stored [k x m]
@@ -135,8 +128,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   if (!ok) return cudaErrorInvalidValue;
   if (g.b_mn)  // B stored [k x n]
     ok = make_map(&mb, g.b, g.n, g.k, g.ldb, 64, 64);
-  else  // B stored [n x k]; with multicast each CTA fetches half the tile's rows
-    ok = make_map(&mb, g.b, g.k, g.n, g.ldb, BK, mc ? BN / 2 : BN);
+  else  // B stored [n x k]
+    ok = make_map(&mb, g.b, g.k, g.n, g.ldb, BK, BN);
   if (!ok) return cudaErrorInvalidValue;
   KParams p{};
   p.m = g.m;
@@ -149,7 +142,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   const int64_t tiles = (int64_t)p.num_m_blocks * p.num_n_blocks;
   if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
   p.num_tiles = (int)tiles;
-  p.m_units = mc ? (p.num_m_blocks + 1) / 2 : p.num_m_blocks;
+  p.m_units = p.num_m_blocks;
   p.num_units = p.m_units * p.num_n_blocks;
   p.raster = g.raster_n_fastest;
   {
@@ -161,7 +154,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
       const long mbb = strtol(b, nullptr, 10);
       if (mbb > 0 && mbb <= 4096) band_bytes = (int64_t)mbb << 20;
     }
-    const int64_t per_unit = (int64_t)BM * (mc ? 2 : 1) * g.k * 2;
+    const int64_t per_unit = (int64_t)BM * g.k * 2;
     int64_t gm = per_unit > 0 ? band_bytes / per_unit : 1;
     if (gm < 1) gm = 1;
     if (gm > p.m_units) gm = p.m_units;
@@ -176,15 +169,15 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.stats = g.stats;
   p.stats_scale = g.stats_scale;
   auto* d = reinterpret_cast<__nv_bfloat16*>(g.d);
-  // split-K when the output has too few tiles for the GPU (one-CTA schedule,
-  // plain stores only); the partials go to the caller's scratch.
+  // split-K when the output has too few tiles for the GPU (plain stores
+  // only); the partials go to the caller's scratch.
   // FLJSD_GEMM_SPLITK=0 in the environment turns it off.
   p.k_splits = 1;
   p.kb_per_split = p.num_k_blocks;
   p.partial = nullptr;
   const char* senv = getenv("FLJSD_GEMM_SPLITK");
   const bool split_off = senv != nullptr && senv[0] == '0';
-  if (!mc && !split_off && g.splitk_ws != nullptr && !g.accumulate && g.d32 == nullptr &&
+  if (!split_off && g.splitk_ws != nullptr && !g.accumulate && g.d32 == nullptr &&
       g.stats == nullptr) {
     int s_ = splitk_factor(g.m, g.n, g.k, num_sms());
     while (s_ > 1 && (size_t)s_ * (size_t)g.m * (size_t)g.ldd * sizeof(float) > g.splitk_ws_bytes)
@@ -273,13 +266,13 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.epi_mode = p.stage_out ? EPI_STAGE
                            : (p.slab_store && !p.slab_f32 ? EPI_SLAB16 : EPI_GENERIC);
   if (p.k_splits > 1) {
-    cudaError_t e = launch_layout(g.a_mn, g.b_mn, false, ma, mb, mcm, msm, d, p, st);
+    cudaError_t e = launch_layout(g.a_mn, g.b_mn, ma, mb, mcm, msm, d, p, st);
     if (e != cudaSuccess) return e;
     k_splitk_reduce<<<num_sms() * 4, 256, 0, st>>>(p.partial, p.k_splits, g.m, g.n, g.ldd, d);
     count_extra_launch();
     return cudaGetLastError();
   }
-  return launch_layout(g.a_mn, g.b_mn, mc, ma, mb, mcm, msm, d, p, st);
+  return launch_layout(g.a_mn, g.b_mn, ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace fljsd

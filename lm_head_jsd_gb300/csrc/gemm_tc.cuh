@@ -35,7 +35,6 @@ struct TcGemmArgs {
   // touched, unless finalize == 1: then D = round(d32 + product).
   float* d32;
   int finalize;
-  int no_multicast;  // 1: one CTA per tile even where a 2-CTA cluster could share B
   // Test of the bounded waits: with stall_producer no copy is issued, so the
   // MMA's first wait expires after timeout_ns (0 = the 10 s default) and the
   // kernel reports FLJSD_ERR_TIMEOUT in *status and exits cleanly.

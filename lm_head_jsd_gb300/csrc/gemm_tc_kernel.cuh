@@ -31,11 +31,8 @@
 // (both K-major), grad_input = dZ . W (B MN-major), grad_weight = dZ^T . X
 // (both MN-major).
 //
-// Pairs of m-blocks can run as a 2-CTA cluster that shares the B tile: each
-// CTA fetches half of it with a TMA multicast into both CTAs, each MMA frees a
-// stage in both CTAs with a multicast commit, and cluster barriers fence the
-// start and the exit. Tile orders: bands of m-blocks sweeping all n-blocks
-// (the band of A stays in L2 while B streams), or n-blocks fastest.
+// Tile orders: bands of m-blocks sweeping all n-blocks (the band of A stays in
+// L2 while B streams), or n-blocks fastest.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the kernel records
 // FLJSD_ERR_TIMEOUT in a device status word, stops issuing work, drains what
@@ -158,16 +155,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Same copy, delivered to the same shared-memory offset (and completing on the
-// same mbarrier offset) in every CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                               int32_t x, int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
 // Shared -> global tensor copy (clipped at the tensor's bounds), tracked by
 // bulk groups of the issuing thread.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
@@ -206,16 +193,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // tcgen05 shared-memory matrix descriptor (sm_100 family):
 // [0,14) start >> 4, [16,30) leading-dimension byte offset >> 4,
 // [32,46) stride-dimension byte offset >> 4, [46,48) version = 1,
@@ -249,14 +226,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-// Arrive on the mbarrier at this offset in every CTA of cta_mask once all
-// previously issued MMAs of this thread have completed.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
       : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -304,8 +273,7 @@ struct KParams {
   float2* stats;       // [m x num_n_blocks] (max, sum 2^(x - max)) per row and tile, or null
   float stats_scale;   // x = bf16(value) * stats_scale
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
-  // scheduling units: m-blocks (one CTA per tile) or pairs of m-blocks (a
-  // 2-CTA cluster per pair, sharing the B tile through multicast)
+  // scheduling units: m-blocks (one CTA per tile)
   int m_units, num_units;
   int raster;   // 0: bands of group_m m-units sweeping all n-blocks; 1: n-blocks fastest
   int group_m;  // m-units per band
@@ -474,7 +442,7 @@ static __device__ __noinline__ void store_chunk_generic(const KParams& p, float*
   }
 }
 
-template <bool A_MN, bool B_MN, bool MC, int G, int EPI>
+template <bool A_MN, bool B_MN, int G, int EPI>
 __global__ void __launch_bounds__(threads_for(G), 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
@@ -491,9 +459,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&cb->full[s]), 1);
-      // with multicast both CTAs' MMAs must have read a stage before either
-      // producer refills it (each producer writes into both CTAs)
-      mbar_init(smem_u32(&cb->empty[s]), MC ? 2 : 1);
+      mbar_init(smem_u32(&cb->empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&cb->tmem_full[a]), 1);
@@ -523,12 +489,8 @@ __global__ void __launch_bounds__(threads_for(G), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = cb->tmem_base;
-  // the peer's multicast copies and commits target this CTA's barriers: they
-  // must be initialised cluster-wide before anyone issues
-  if (MC) cluster_sync_all();
-  const uint32_t rank = MC ? cluster_ctarank() : 0u;
-  const int unit0 = MC ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int unit_step = MC ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int unit0 = (int)blockIdx.x;
+  const int unit_step = (int)gridDim.x;
 
   // Tile order. n-fastest: all n-blocks of a few m-blocks run together (used
   // when B is small and A streams). Grouped: bands of group_m m-blocks; inside
@@ -547,7 +509,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
       mu = m0 + r % gm;
       nb = r / gm;
     }
-    mb = MC ? 2 * mu + (int)rank : mu;
+    mb = mu;
   };
   auto unit_split = [&](int t, int& tile, int& split, int& kb0, int& kb1) {
     if (p.k_splits > 1) {
@@ -593,17 +555,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
           } else {
             tma_load_2d(sa, &tmA, fb, k0, m0);
           }
-          if (MC) {
-            // this CTA fetches half of the B tile for both CTAs of the pair
-            if (B_MN) {
-#pragma unroll
-              for (int j = 2 * (int)rank; j < 2 * (int)rank + 2; ++j)
-                tma_load_2d_mc(sb + j * 8192, &tmB, fb, n0 + 64 * j, k0, (uint16_t)3);
-            } else {
-              tma_load_2d_mc(sb + rank * (B_BYTES / 2), &tmB, fb, k0, n0 + (int)rank * (BN / 2),
-                             (uint16_t)3);
-            }
-          } else if (B_MN) {
+          if (B_MN) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tmB, fb, n0 + 64 * j, k0);
           } else {
@@ -659,11 +611,8 @@ __global__ void __launch_bounds__(threads_for(G), 1)
               bd = smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
             mma_bf16(tmem_d, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          // frees the stage once read (in both CTAs of a multicast pair)
-          if (MC)
-            mma_commit_mc(smem_u32(&cb->empty[stage]), (uint16_t)3);
-          else
-            mma_commit(smem_u32(&cb->empty[stage]));
+          // frees the stage once read
+          mma_commit(smem_u32(&cb->empty[stage]));
           any = true;
           if (++stage == p.nst) {
             stage = 0;
@@ -940,9 +889,6 @@ __global__ void __launch_bounds__(threads_for(G), 1)
 
   tc_fence_before();
   __syncthreads();
-  // no CTA of a pair leaves while its peer may still write into its shared
-  // memory or arrive on its barriers
-  if (MC) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -951,76 +897,48 @@ __global__ void __launch_bounds__(threads_for(G), 1)
   }
 }
 
-template <bool A_MN, bool B_MN, bool MC, int G, int EPI>
+template <bool A_MN, bool B_MN, int G, int EPI>
 cudaError_t launch_g(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mcm,
                      const CUtensorMap& msm, __nv_bfloat16* d, KParams p, cudaStream_t st) {
   constexpr int THREADS = threads_for(G);
   const int smem = smem_bytes(p.nst, p.nslab, p.stage_out ? 4 * G * p.nbuf : 0);
-  static int max_clusters[64] = {0};
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   const bool cache = dev >= 0 && dev < 64;
-  auto kern = k_gemm_tc<A_MN, B_MN, MC, G, EPI>;
+  auto kern = k_gemm_tc<A_MN, B_MN, G, EPI>;
   if (!cache || !attr_set[dev]) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
     if (e != cudaSuccess) return e;
     if (cache) attr_set[dev] = true;
   }
-  if (!MC) {
-    const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
-    kern<<<grid, THREADS, smem, st>>>(ma, mb, mcm, msm, d, p);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // a persistent grid must not exceed the clusters that can be resident at once
-  if (!cache || max_clusters[dev] == 0) {
-    int n = 0;
-    cfg.gridDim = dim3(2 * (num_sms() / 2));
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = 1;
-    if (cache) max_clusters[dev] = n;
-    else max_clusters[0] = n;
-  }
-  const int mc = cache ? max_clusters[dev] : max_clusters[0];
-  const int clusters = p.num_units < mc ? p.num_units : mc;
-  cfg.gridDim = dim3(2 * clusters);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mcm, msm, d, p);
-  if (e != cudaSuccess) return e;
+  const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
+  kern<<<grid, THREADS, smem, st>>>(ma, mb, mcm, msm, d, p);
   return cudaGetLastError();
 }
 
-// Every (epilogue groups, epilogue mode) variant of one layout and schedule.
-template <bool A_MN, bool B_MN, bool MC>
+// Every (epilogue groups, epilogue mode) variant of one layout.
+template <bool A_MN, bool B_MN>
 cudaError_t launch_modes(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mcm,
                          const CUtensorMap& msm, __nv_bfloat16* d, const KParams& p,
                          cudaStream_t st) {
   if (p.epi_groups == 2) {
-    if (p.epi_mode == EPI_STAGE) return launch_g<A_MN, B_MN, MC, 2, EPI_STAGE>(ma, mb, mcm, msm, d, p, st);
-    if (p.epi_mode == EPI_SLAB16) return launch_g<A_MN, B_MN, MC, 2, EPI_SLAB16>(ma, mb, mcm, msm, d, p, st);
-    return launch_g<A_MN, B_MN, MC, 2, EPI_GENERIC>(ma, mb, mcm, msm, d, p, st);
+    if (p.epi_mode == EPI_STAGE) return launch_g<A_MN, B_MN, 2, EPI_STAGE>(ma, mb, mcm, msm, d, p, st);
+    if (p.epi_mode == EPI_SLAB16) return launch_g<A_MN, B_MN, 2, EPI_SLAB16>(ma, mb, mcm, msm, d, p, st);
+    return launch_g<A_MN, B_MN, 2, EPI_GENERIC>(ma, mb, mcm, msm, d, p, st);
   }
-  if (p.epi_mode == EPI_STAGE) return launch_g<A_MN, B_MN, MC, 1, EPI_STAGE>(ma, mb, mcm, msm, d, p, st);
-  if (p.epi_mode == EPI_SLAB16) return launch_g<A_MN, B_MN, MC, 1, EPI_SLAB16>(ma, mb, mcm, msm, d, p, st);
-  return launch_g<A_MN, B_MN, MC, 1, EPI_GENERIC>(ma, mb, mcm, msm, d, p, st);
+  if (p.epi_mode == EPI_STAGE) return launch_g<A_MN, B_MN, 1, EPI_STAGE>(ma, mb, mcm, msm, d, p, st);
+  if (p.epi_mode == EPI_SLAB16) return launch_g<A_MN, B_MN, 1, EPI_SLAB16>(ma, mb, mcm, msm, d, p, st);
+  return launch_g<A_MN, B_MN, 1, EPI_GENERIC>(ma, mb, mcm, msm, d, p, st);
 }
 
 // Launchers of one operand layout (A K-major or MN-major, B likewise), each
-// defined in its own translation unit: every schedule (2-CTA pairs or one CTA
-// per tile; one or two epilogue groups, from p.epi_groups).
+// defined in its own translation unit: every epilogue variant (one or two
+// epilogue groups, from p.epi_groups).
 #define FLJSD_TC_LAUNCHER(name)                                                    \
   cudaError_t name(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mcm, \
-                   const CUtensorMap& msm, __nv_bfloat16* d, const KParams& p, bool mc, \
+                   const CUtensorMap& msm, __nv_bfloat16* d, const KParams& p,    \
                    cudaStream_t st)
 FLJSD_TC_LAUNCHER(launch_kk);
 FLJSD_TC_LAUNCHER(launch_kmn);

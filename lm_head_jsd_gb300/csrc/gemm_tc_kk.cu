@@ -5,8 +5,7 @@ namespace fljsd {
 namespace tcgemm {
 
 FLJSD_TC_LAUNCHER(launch_kk) {
-  return mc ? launch_modes<false, false, true>(ma, mb, mcm, msm, d, p, st)
-            : launch_modes<false, false, false>(ma, mb, mcm, msm, d, p, st);
+  return launch_modes<false, false>(ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace tcgemm

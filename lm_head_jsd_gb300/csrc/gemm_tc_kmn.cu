@@ -5,8 +5,7 @@ namespace fljsd {
 namespace tcgemm {
 
 FLJSD_TC_LAUNCHER(launch_kmn) {
-  return mc ? launch_modes<false, true, true>(ma, mb, mcm, msm, d, p, st)
-            : launch_modes<false, true, false>(ma, mb, mcm, msm, d, p, st);
+  return launch_modes<false, true>(ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace tcgemm

@@ -5,8 +5,7 @@ namespace fljsd {
 namespace tcgemm {
 
 FLJSD_TC_LAUNCHER(launch_mnmn) {
-  return mc ? launch_modes<true, true, true>(ma, mb, mcm, msm, d, p, st)
-            : launch_modes<true, true, false>(ma, mb, mcm, msm, d, p, st);
+  return launch_modes<true, true>(ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace tcgemm

@@ -92,6 +92,34 @@ def test_planner_fits_free_memory(L):
     assert e.value.status == 3
 
 
+def test_planner_fp32_accumulator_only_charged_to_chunked_plans(L):
+    """With FLJSD_FLAG_ACCUM_FP32 the V x H fp32 grad_weight accumulator is
+    needed only when there is more than one chunk (PR 1429's accum_dtype
+    option accumulates across chunks). A budget that holds the one-chunk
+    workspace but not the accumulator must give one chunk, not an error."""
+    p = L.make_problem(64, 4096, 4096, 128256, "bf16", accum_fp32=True)
+    single = L.fljsd_plan(p, 0)
+    assert single.chunk_rows == 64 and single.num_chunks == 1
+    acc_bytes = 128256 * 4096 * 4
+    assert single.workspace_bytes < acc_bytes  # the one-chunk plan carries no accumulator
+    plan = L.fljsd_plan(p, 2 * single.workspace_bytes)  # half of it is the budget
+    assert plan.chunk_rows == 64 and plan.num_chunks == 1
+    assert plan.workspace_bytes == single.workspace_bytes
+    # the same budget without the flag gives the same plan
+    q = L.make_problem(64, 4096, 4096, 128256, "bf16")
+    assert L.fljsd_plan(q, 2 * single.workspace_bytes).workspace_bytes == single.workspace_bytes
+    # a multi-chunk plan does carry it: it needs more than the accumulator
+    big = L.make_problem(8192, 4096, 4096, 128256, "bf16", accum_fp32=True)
+    one_chunk = L.fljsd_plan(big, 0).workspace_bytes
+    chunked = L.fljsd_plan(big, one_chunk)  # half of one chunk's workspace
+    assert chunked.num_chunks > 1 and chunked.workspace_bytes > acc_bytes
+    assert chunked.workspace_bytes <= one_chunk // 2
+    # a budget below the accumulator cannot hold any chunked plan
+    with pytest.raises(L.FljsdError) as e:
+        L.fljsd_plan(big, acc_bytes)
+    assert e.value.status == 3
+
+
 @pytest.mark.parametrize("field,value", [
     ("bt", 0), ("h_s", -1), ("h_t", 0), ("v", 0), ("dtype", 7), ("reduction", 9),
     ("beta", 1.5), ("beta", -0.1), ("beta", float("nan")), ("temperature", 0.0),
