@@ -70,6 +70,11 @@ WORKLOADS = {
     "headline": Workload("headline", 6, 8192, 4096, 4096, 128256, "bf16"),
     # the headline's H and V with BT=1024 (small enough for full profiler captures)
     "headline_bt1024": Workload("headline_bt1024", 7, 1024, 4096, 4096, 128256, "bf16"),
+    # the headline's BT and H with a quarter of V (about 2 GB on the device):
+    # every kernel of a step keeps the headline's schedule, and its work and
+    # traffic per launch scale with V, so profiler counters taken here scale
+    # to the headline by 4
+    "headline_v32k": Workload("headline_v32k", 8, 8192, 4096, 4096, 32064, "bf16"),
 }
 
 
@@ -143,6 +148,72 @@ def custom(name: str, seed: int, bt: int, h_s: int, v: int, dtype: str = "bf16",
            h_t: int | None = None, **kw) -> Workload:
     """A workload of arbitrary shape with the same recipe (for small and odd shapes)."""
     return Workload(name, seed, bt, h_s, h_s if h_t is None else h_t, v, dtype, **kw)
+
+
+def make_partial_ties(bt: int, h: int, v: int, dtype: str, seed: int, *, temperature: float,
+                      diff_cols, n_full: int, n_free: int, ignore_frac: float = 0.0,
+                      device: str = "cpu"):
+    """Inputs whose rows tie (student and teacher log-probabilities exactly
+    equal) at most columns but not all.
+
+    Ties that hold exactly in any arithmetic need bitwise-equal log-normalisers
+    on both sides, so the logits of the two models agree everywhere except in
+    a few columns ``diff_cols`` whose logits lie so far below the row maximum
+    (about 45 scaled units) that they cannot change a float64 or float32 sum of
+    exponentials, yet still give normal float32 probabilities:
+
+    * X_s ~ N(0, 1) [BT x H] and W_s ~ N(0, 1/H) [V x H] in float32, drawn in
+      that order from a generator seeded with ``seed``; hidden column 0 of W_s
+      is then set to 0.
+    * Vocabulary rows ``diff_cols`` of W_s are 0 except hidden column 0, which
+      is c_s; in W_t = W_s it is c_t. With X[:, 0] = 8 their logits are exactly
+      8 c_s and 8 c_t (representable in bf16): c_s, c_t = -5, -4.5 at T = 1
+      and -12, -11 at T = 2 (scaled logits -40 / -36 and -48 / -44).
+    * Row kinds (a seeded permutation scatters them): "partial" rows have
+      X_t = X_s and X[:, 0] = 8, so they tie everywhere except ``diff_cols``;
+      ``n_full`` "full" rows have X[:, 0] = 0, so every logit of both models
+      is equal and the row ties everywhere; ``n_free`` "free" rows get an
+      independent teacher row X_t ~ N(0, 1) (X_t[:, 0] = 8), so they tie
+      nowhere and carry ordinary loss and gradient.
+    * Labels as in make_labels (``ignore_frac`` of the rows ignored).
+
+    Returns ((x_s, w_s, x_t, w_t, labels), kinds) with kinds an array of
+    "partial" / "full" / "free" per row.
+    """
+    import numpy as np
+
+    if temperature == 1.0:
+        c_s, c_t = -5.0, -4.5
+    elif temperature == 2.0:
+        c_s, c_t = -12.0, -11.0
+    else:
+        raise ValueError("the construction is calibrated for T = 1 and T = 2")
+    gen = torch.Generator(device=device).manual_seed(seed)
+    x_s = _randn((bt, h), 1.0, gen, device)
+    w_s = _randn((v, h), 1.0 / math.sqrt(h), gen, device)
+    x_free = _randn((bt, h), 1.0, gen, device)
+    perm = torch.randperm(bt, generator=torch.Generator().manual_seed(seed + 1))
+    kinds = np.array(["partial"] * bt, dtype=object)
+    full = perm[:n_full]
+    free = perm[n_full:n_full + n_free]
+    kinds[full.numpy()] = "full"
+    kinds[free.numpy()] = "free"
+    cols = torch.as_tensor(list(diff_cols), dtype=torch.int64)
+    w_s[:, 0] = 0.0
+    w_s[cols] = 0.0
+    w_t = w_s.clone()
+    w_s[cols, 0] = c_s
+    w_t[cols, 0] = c_t
+    x_s[:, 0] = 8.0
+    x_s[full.to(device), 0] = 0.0
+    x_t = x_s.clone()
+    x_t[free.to(device)] = x_free[free.to(device)]
+    x_t[free.to(device), 0] = 8.0
+    dt = torch.float32 if dtype == "fp32" else torch.bfloat16
+    labels = make_labels(bt, v, ignore_frac, seed)
+    if labels is not None:
+        labels = labels.to(device)
+    return (x_s.to(dt), w_s.to(dt), x_t.to(dt), w_t.to(dt), labels), kinds
 
 
 def make_distributions(rows: int, v: int, dtype: str, seed: int, *, logspace: bool,

@@ -7,6 +7,7 @@ the product library.
 from .fljsd_oracle import (  # noqa: F401
     REDUCTIONS,
     bf16_round,
+    dist_zero_masks,
     fljsd_from_logits,
     fljsd_ref,
     fljsd_rows_ref,
@@ -16,5 +17,7 @@ from .fljsd_oracle import (  # noqa: F401
     log_softmax_rows,
     logits,
     row_weights,
+    tie_mask,
     tvd_ref,
+    zero_masks,
 )

@@ -103,6 +103,42 @@ def log_softmax_rows(a: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # per-row JSD and its gradient with respect to the scaled student logits
 # ---------------------------------------------------------------------------
+def tie_mask(z_s: np.ndarray, z_t: np.ndarray, temperature: float) -> np.ndarray:
+    """Elements where the student and teacher log-probabilities are exactly
+    equal, X_j == Y_j (the tie rule of PR 1374 "Summary": such an element
+    contributes exactly zero). Shape [rows x V], boolean."""
+    a = np.asarray(z_s, dtype=np.float64) / temperature
+    b = np.asarray(z_t, dtype=np.float64) / temperature
+    return log_softmax_rows(a) == log_softmax_rows(b)
+
+
+def zero_masks(z_s, z_t, labels, beta: float, temperature: float, ignore_index: int = -100):
+    """Where the method itself gives exact zeros (not where a float result
+    happens to cancel), for rows whose logits are z_s, z_t.
+
+    Returns (loss_zero [rows], dz_zero [rows x V]):
+    * ignored rows: loss 0 and dlogits 0 (reading of ignore_index);
+    * rows tied at every element: every per-element loss is 0, so L = 0, and
+      the logit gradient is 0 in every branch (beta = 0: Q - P = 0; beta = 1:
+      Q (X - Y - L) = 0; generalized: dX = 0 at every element, so dX_sum = 0);
+    * beta = 0: dlogits (Q - P) / T is exactly 0 at every tied element of any
+      row, since Q == P there (PR 1374 "Summary" carried to the logit gradient
+      by PR 1352 "Details"). In the other branches a tied element of an
+      untied row has the nonzero gradient -Q_j L (beta = 1) or -Q_j dX_sum.
+    """
+    tie = tie_mask(z_s, z_t, temperature)
+    rows = tie.shape[0]
+    valid = np.ones(rows, dtype=bool) if labels is None else \
+        np.asarray(labels).reshape(-1) != ignore_index
+    full = np.all(tie, axis=1)
+    loss_zero = ~valid | full
+    dz_zero = np.zeros_like(tie)
+    if beta == 0.0:
+        dz_zero |= tie
+    dz_zero[loss_zero] = True
+    return loss_zero, dz_zero
+
+
 def jsd_rows(z_s: np.ndarray, z_t: np.ndarray, beta: float, temperature: float):
     """Per-row loss L_r (shape [rows]) and dA = dL_r/da (shape [rows x V]).
 
@@ -126,7 +162,7 @@ def jsd_rows(z_s: np.ndarray, z_t: np.ndarray, beta: float, temperature: float):
     Y = log_softmax_rows(b)
     Q = np.exp(X)
     P = np.exp(Y)
-    tie = X == Y
+    tie = X == Y  # the same test as tie_mask
     if beta == 0.0:
         # forward KL(P || Q)
         ell = np.where(tie, 0.0, P * (Y - X))
@@ -338,6 +374,35 @@ def tvd_ref(p: np.ndarray, q: np.ndarray, reduction: str = "batchmean", labels=N
         return 0.0, grad
     scale = {"sum": 1.0, "batchmean": 1.0 / n, "mean": 1.0 / (n * v)}[reduction]
     return float(total * scale), grad
+
+
+def dist_zero_masks(kind: str, x: np.ndarray, y: np.ndarray, *, beta: float = 0.5,
+                    labels=None, ignore_index: int = -100):
+    """Exact zeros of the two distances over given distributions, from the tie
+    rule of PR 1374 "Summary" (x == y element by element) and the ignored rows.
+
+    kind "tvd": the gradient 0.5 sign(p - q) is 0 at p == q, and the
+    per-element loss 0.5 |p - q| is 0 there. kind "jsd" (log-space): the
+    per-element loss is 0 at X == Y in every branch; the gradient is 0 there
+    only in the generalized branch ((1 - beta) Q (X - log M), with M = Q);
+    the endpoint gradients -P and Q (X - Y + 1) are not 0 at a tie.
+    Returns (elem_loss_zero [rows x V], grad_zero [rows x V]); ignored rows are
+    all True.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    tie = x == y
+    rows = x.shape[0]
+    valid = np.ones(rows, dtype=bool) if labels is None else \
+        np.asarray(labels).reshape(-1) != ignore_index
+    loss_zero = tie.copy()
+    if kind == "tvd" or (0.0 < beta < 1.0):
+        grad_zero = tie.copy()
+    else:
+        grad_zero = np.zeros_like(tie)
+    loss_zero[~valid] = True
+    grad_zero[~valid] = True
+    return loss_zero, grad_zero
 
 
 def jsd_logspace_ref(x: np.ndarray, y: np.ndarray, *, beta: float = 0.5,

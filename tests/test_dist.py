@@ -7,7 +7,7 @@ import torch
 
 import jsd_inputs
 import oracle
-from parity_util import TOL, assert_zeros_where_ref_zero, f64, rel_fro
+from parity_util import TOL, assert_exact_zeros, f64, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -34,16 +34,26 @@ def _run(kind, a, b, labels, dtype, reduction, beta=0.5):
     return loss, grad
 
 
-def _check(loss, grad, ref, dtype, what):
+def _check(loss, grad, ref, dtype, what, zeros):
+    """Tolerances as for the fused loss; ``zeros`` = oracle.dist_zero_masks:
+    where the method gives exact zeros (ties, ignored rows) the kernel must
+    give 0.0 -- per element for the gradient and for TVD's per-element loss,
+    per row (rows tied everywhere or ignored) for a per-row loss."""
     tol_loss, tol_grad = TOL[dtype]
     rl = np.atleast_1d(np.asarray(ref[0], dtype=np.float64))
     gl = f64(loss).reshape(rl.shape)
     if np.any(rl != 0.0):
         assert rel_fro(gl, rl) <= tol_loss, (what, rel_fro(gl, rl))
-    assert_zeros_where_ref_zero(gl, rl, what + " loss")
+    else:
+        assert np.all(gl == 0.0), what
+    elem_zero, grad_zero = zeros
+    if gl.shape == elem_zero.shape:
+        assert_exact_zeros(gl, elem_zero, what + " loss")
+    elif gl.shape == elem_zero.shape[:1]:
+        assert_exact_zeros(gl, np.all(elem_zero, axis=1), what + " loss rows")
     gg = f64(grad)
     assert np.all(np.isfinite(gg))
-    assert_zeros_where_ref_zero(gg, ref[1], what + " grad")
+    assert_exact_zeros(gg, grad_zero, what + " grad")
     if np.any(ref[1] != 0.0):
         assert rel_fro(gg, ref[1]) <= tol_grad, (what, rel_fro(gg, ref[1]))
 
@@ -59,9 +69,10 @@ def test_jsd_logspace(shape, dtype, beta):
                                                  ignore_frac=0.1 if rows >= 10 else 0.0)
     for red in ("none", "sum", "mean", "batchmean"):
         loss, grad = _run("jsd", a, b, labels, dtype, red, beta)
-        ref = oracle.jsd_logspace_ref(f64(a), f64(b), beta=beta, reduction=red,
-                                      labels=None if labels is None else labels.numpy())
-        _check(loss, grad, ref, dtype, f"jsd {shape} {dtype} beta={beta} {red}")
+        lab = None if labels is None else labels.numpy()
+        ref = oracle.jsd_logspace_ref(f64(a), f64(b), beta=beta, reduction=red, labels=lab)
+        zeros = oracle.dist_zero_masks("jsd", f64(a), f64(b), beta=beta, labels=lab)
+        _check(loss, grad, ref, dtype, f"jsd {shape} {dtype} beta={beta} {red}", zeros)
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"{s[0]}x{s[1]}")
@@ -74,9 +85,10 @@ def test_tvd(shape, dtype):
                                                  ignore_frac=0.1 if rows >= 10 else 0.0)
     for red in ("none", "sum", "mean", "batchmean"):
         loss, grad = _run("tvd", a, b, labels, dtype, red)
-        ref = oracle.tvd_ref(f64(a), f64(b), reduction=red,
-                             labels=None if labels is None else labels.numpy())
-        _check(loss, grad, ref, dtype, f"tvd {shape} {dtype} {red}")
+        lab = None if labels is None else labels.numpy()
+        ref = oracle.tvd_ref(f64(a), f64(b), reduction=red, labels=lab)
+        zeros = oracle.dist_zero_masks("tvd", f64(a), f64(b), labels=lab)
+        _check(loss, grad, ref, dtype, f"tvd {shape} {dtype} {red}", zeros)
         # the gradient is exactly +-0.5 w or 0: compare it exactly
         assert np.array_equal(f64(grad), ref[1].astype(np.float32).astype(
             np.float64) if dtype == "fp32" else f64(torch.from_numpy(ref[1]).to(torch.bfloat16)))

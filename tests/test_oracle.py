@@ -299,6 +299,98 @@ def test_finite_differences_at_partial_ties(beta):
 
 
 # ---------------------------------------------------------------------------
+# the tie mask and the method's exact zeros
+# ---------------------------------------------------------------------------
+def _partial_tie_logits():
+    """Row 0: the teacher equals the student except at column 3, where both
+    logits sit 60 units below the row maximum (too small to move a float64
+    sum of exponentials), so the log-normalisers are bitwise equal and every
+    other column ties. Row 1: equal everywhere. Row 2: independent."""
+    r = _rng(41)
+    v = 10
+    zs = r.standard_normal((3, v))
+    zt = zs.copy()
+    zs[0, 3] = zs[0].max() - 60.0
+    zt[0, 3] = zs[0].max() - 58.0
+    zt[2] = r.standard_normal(v)
+    return zs, zt
+
+
+def test_tie_mask_on_constructed_partial_ties():
+    from oracle import tie_mask
+
+    zs, zt = _partial_tie_logits()
+    m = tie_mask(zs, zt, 1.0)
+    expect = np.ones_like(m)
+    expect[0, 3] = False
+    expect[2] = False
+    assert np.array_equal(m, expect)
+    # a temperature that keeps column 3 far below the maximum keeps the ties
+    assert np.array_equal(tie_mask(zs, zt, 1.5), expect)
+
+
+@pytest.mark.parametrize("beta", BETAS)
+def test_zero_masks_are_the_exact_zeros(beta):
+    """The mask marks exactly the zeros the tie rule and ignored rows fix: the
+    oracle's logit gradient is 0.0 there, and the tied elements of the
+    partially tied row are left unmarked (and nonzero) outside beta = 0,
+    where their gradient is -Q L (beta = 1) or -Q dX_sum."""
+    from oracle import zero_masks
+
+    zs, zt = _partial_tie_logits()
+    labels = np.array([5, 1, 2, -100])
+    zs = np.vstack([zs, zs[2]])
+    zt = np.vstack([zt, zt[2]])
+    loss_zero, dz_zero = zero_masks(zs, zt, labels, beta, 1.0)
+    assert loss_zero.tolist() == [False, True, False, True]
+    L, dA = jsd_rows(zs, zt, beta, 1.0)
+    valid = labels != -100
+    dA[~valid] = 0.0
+    assert np.all(dA[dz_zero] == 0.0)
+    assert np.all(L[1] == 0.0)
+    tied_cols = np.ones(zs.shape[1], bool)
+    tied_cols[3] = False
+    assert np.all(dz_zero[1]) and np.all(dz_zero[3])
+    if beta == 0.0:
+        assert np.all(dz_zero[0, tied_cols]) and not dz_zero[0, 3]
+    else:
+        assert not np.any(dz_zero[0])
+        assert np.all(dA[0, tied_cols] != 0.0)
+    assert not np.any(dz_zero[2])
+
+
+def test_dist_zero_masks():
+    """TVD: the gradient is 0 exactly where p == q (PR 1374 "Summary"); the
+    log-space JSD: every branch's loss term is 0 at a tie, the gradient only in
+    the generalized branch (the endpoints' -P and Q (X - Y + 1) are not 0)."""
+    from oracle import dist_zero_masks, jsd_logspace_ref
+
+    r = _rng(43)
+    p = r.random((3, 6)) + 0.1
+    q = p.copy()
+    q[0, [1, 4]] += 0.05
+    q[2] = r.random(6) + 0.1
+    labels = np.array([0, -100, 1])
+    lz, gz = dist_zero_masks("tvd", p, q, labels=labels)
+    ties = p == q
+    assert np.array_equal(gz[[0, 2]], ties[[0, 2]]) and np.all(gz[1])
+    _, g = tvd_ref(p, q, reduction="sum", labels=labels)
+    assert np.all(g[gz] == 0.0) and np.all(g[~gz] != 0.0)
+    x = np.log(p / p.sum(axis=1, keepdims=True))
+    y = np.log(q / q.sum(axis=1, keepdims=True))
+    y[0] = x[0]
+    y[0, 2] -= 0.3
+    for beta in BETAS:
+        lz, gz = dist_zero_masks("jsd", x, y, beta=beta, labels=labels)
+        _, g = jsd_logspace_ref(x, y, beta=beta, reduction="sum", labels=labels)
+        assert np.all(g[gz] == 0.0)
+        if beta in (0.0, 1.0):
+            assert not np.any(gz[0]) and np.all(g[0] != 0.0)
+        else:
+            assert np.array_equal(gz[0], x[0] == y[0])
+
+
+# ---------------------------------------------------------------------------
 # the printed value: the TVD tie table pins batchmean = divide by rows
 # ---------------------------------------------------------------------------
 def _golden(name):

@@ -8,7 +8,8 @@ import torch
 
 import jsd_inputs
 import oracle
-from parity_util import TOL, compare, f64, rel_fro, run_gpu
+from parity_util import (TOL, assert_exact_zeros, compare, f64, method_zeros, oracle_zeros,
+                         rel_fro, run_gpu, tile_errors)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,7 +36,10 @@ def tiny():
 def test_tiny_fp32(tiny, beta, T, red):
     out = run_gpu(*tiny, beta=beta, temperature=T, reduction=red)
     ref = _oracle(tiny, beta=beta, temperature=T, reduction=red)
-    compare(out, ref, "fp32", f"tiny beta={beta} T={T} {red}")
+    compare(out, ref, "fp32", f"tiny beta={beta} T={T} {red}",
+            zeros=oracle_zeros(tiny, beta, T))
+    for k, e in tile_errors(f64(out[2]), ref[2], 1000).items():
+        assert e <= TOL["fp32"][1], (k, e)
 
 
 # ---------------------------------------------------------------------------
@@ -59,7 +63,97 @@ def test_padded_vocab():
     inputs = jsd_inputs.make_inputs(w, "cpu")
     out = run_gpu(*inputs, beta=w.beta, temperature=w.temperature, reduction=w.reduction)
     ref = _oracle(inputs, beta=w.beta, temperature=w.temperature, reduction=w.reduction)
-    compare(out, ref, "bf16", "padded vocab")
+    compare(out, ref, "bf16", "padded vocab",
+            zeros=oracle_zeros(inputs, w.beta, w.temperature))
+
+
+# ---------------------------------------------------------------------------
+# partially tied rows: the tie rule element by element
+# ---------------------------------------------------------------------------
+PARTIAL_CASES = {
+    # name: (bt, h, v, dtype)
+    "fp32_v1000": (64, 128, 1000, "fp32"),
+    "bf16_v40960": (512, 256, 40960, "bf16"),
+    "bf16_v33000": (384, 192, 33000, "bf16"),  # ragged last GEMM and pass-1 tiles
+}
+
+
+def _diff_cols(v):
+    """Columns where student and teacher differ: tile edges of both the
+    256-column GEMM tiles and the 128-column pass-1 partials, the last
+    columns, and one inside."""
+    return sorted({0, 127, 128, 255, 256, v // 2 + 3, v - 129, v - 128, v - 1})
+
+
+@pytest.mark.parametrize("beta", BETAS)
+@pytest.mark.parametrize("case", list(PARTIAL_CASES))
+def test_partial_ties(case, beta):
+    """Rows that tie at every column but a few (jsd_inputs.make_partial_ties),
+    rows tied everywhere, rows tied nowhere, and ignored rows. The tie rule
+    (PR 1374 "Summary"; carried to the logit gradient by PR 1352 "Details")
+    fixes exact zeros that the oracle's tie mask locates: at beta = 0 every
+    tied element's dlogit (Q - P)/T is exactly 0; rows tied everywhere and
+    ignored rows are exactly 0 in every branch. The dlogits are read where the
+    method leaves them, in place over the student logits in the workspace
+    (one chunk). The tied elements of partially tied rows in the other
+    branches (-Q L, -Q dX_sum: tiny but not 0) and the untied columns are
+    compared with the oracle, as are the grad_weight rows at the kernels'
+    tile edges and in the last vocabulary tile."""
+    from lm_head_jsd_gb300 import FusedLinearJSD
+
+    bt, h, v, dt = PARTIAL_CASES[case]
+    tol_loss, tol_grad = TOL[dt]
+    D = _diff_cols(v)
+    for T in (1.0, 2.0):
+        inputs, kinds = jsd_inputs.make_partial_ties(
+            bt, h, v, dt, 91 + v % 97, temperature=T, diff_cols=D, n_full=bt // 16,
+            n_free=bt // 8, ignore_frac=0.1)
+        x_s, w_s, x_t, w_t, labels = (f64(t) for t in inputs)
+        zs, zt = oracle.logits(x_s, w_s), oracle.logits(x_t, w_t)
+        zeros = method_zeros(zs, zt, labels, beta, T)
+        valid = labels != -100
+        part = (kinds == "partial") & valid
+        # the construction: partial rows tie off D and nowhere on D
+        tie = oracle.tie_mask(zs, zt, T)
+        off = np.ones(v, bool)
+        off[D] = False
+        assert np.all(tie[part][:, off]) and not np.any(tie[part][:, D])
+        assert np.all(tie[kinds == "full"]) and not np.any(tie[kinds == "free"])
+
+        dev_in = [t.cuda() for t in inputs]
+        for red in ("batchmean", "none"):
+            run = FusedLinearJSD(bt, h, h, v, inputs[0].dtype, beta=beta, temperature=T,
+                                 reduction=red)
+            assert run.plan.num_chunks == 1
+            out = run.forward(*dev_in)
+            torch.cuda.synchronize()
+            what = f"{case} beta={beta} T={T} {red}"
+            ref = oracle.fljsd_from_logits(zs, zt, x_s, w_s, labels, beta=beta, temperature=T,
+                                           reduction=red)
+            compare(out, ref, dt, what, zeros=zeros)
+            # the dlogits, in place over the student logits (row stride ld)
+            ld = run.plan.ld
+            dz = f64(run.workspace[: bt * ld * inputs[0].element_size()]
+                     .view(inputs[0].dtype).view(bt, ld)[:, :v])
+            assert_exact_zeros(dz, zeros["dz"], what + " dlogits")
+            if beta == 0.0:
+                assert np.all(dz[part][:, off] == 0.0)  # tied elements of untied rows
+            w_r, _, _ = oracle.row_weights(labels, bt, v, red)
+            _, dA = oracle.jsd_rows(zs, zt, beta, T)
+            dz_ref = dA * (w_r / T)[:, None]
+            dz_ref[~valid] = 0.0
+            e = rel_fro(dz[part][:, D], dz_ref[part][:, D])
+            assert e <= tol_grad, f"{what}: dlogits at the untied columns {e:.3g}"
+            if beta != 0.0:
+                e = rel_fro(dz[part][:, off], dz_ref[part][:, off])
+                assert e <= tol_grad, f"{what}: dlogits at tied columns {e:.3g}"
+            for k, e in tile_errors(f64(out[2]), ref[2], v).items():
+                assert e <= tol_grad, f"{what}: grad_weight {k} {e:.3g}"
+            if beta == 0.0:
+                # grad_input of a partially tied row draws only on the untied
+                # columns, whose weight rows are 0 past hidden column 0
+                gi = f64(out[1])
+                assert np.all(gi[part][:, 1:] == 0.0)
 
 
 # ---------------------------------------------------------------------------
@@ -83,7 +177,10 @@ def test_multiblock_sweep(multiblock, beta, T, red):
     out = run_gpu(*inputs, beta=beta, temperature=T, reduction=red)
     ref = oracle.fljsd_from_logits(zs, zt, x_s, w_s, labels, beta=beta, temperature=T,
                                    reduction=red)
-    compare(out, ref, "bf16", f"multiblock beta={beta} T={T} {red}")
+    what = f"multiblock beta={beta} T={T} {red}"
+    compare(out, ref, "bf16", what, zeros=method_zeros(zs, zt, labels, beta, T))
+    for k, e in tile_errors(f64(out[2]), ref[2], zs.shape[1]).items():
+        assert e <= TOL["bf16"][1], f"{what}: grad_weight {k} {e:.3g}"
 
 
 # ---------------------------------------------------------------------------
@@ -103,10 +200,13 @@ def test_small_shapes(shape, beta):
     bt, h, v, dt = shape
     w = jsd_inputs.custom("small", 11 + bt + v, bt, h, v, dt, ignore_frac=0.25 if bt >= 4 else 0.0)
     inputs = jsd_inputs.make_inputs(w, "cpu")
+    zeros = oracle_zeros(inputs, beta, 1.3)
     for red in ("none", "batchmean"):
         out = run_gpu(*inputs, beta=beta, temperature=1.3, reduction=red)
         ref = _oracle(inputs, beta=beta, temperature=1.3, reduction=red)
-        compare(out, ref, dt, f"{shape} beta={beta} {red}")
+        compare(out, ref, dt, f"{shape} beta={beta} {red}", zeros=zeros)
+        for k, e in tile_errors(f64(out[2]), ref[2], v).items():
+            assert e <= TOL[dt][1], (shape, red, k, e)
 
 
 @pytest.mark.parametrize("chunk", [1, 7, 64, 128, 300])
