@@ -372,6 +372,7 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
   const bool stall = (flags & FLJSD_GEMM_TEST_STALL) != 0;
   TcGemmArgs t{a,       lda,  a_mn, b, ldb, b_mn, d, ldd, m, n, k, accumulate, 1, status,
                nullptr, 0.f,  nullptr, 0, stall ? 50ull * 1000 * 1000 : 0ull, stall ? 1 : 0};
+  t.single_cta = (flags & FLJSD_GEMM_SINGLE_CTA) ? 1 : 0;
   if (!tc_gemm_supported(t)) return FLJSD_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   trace_begin(FLJSD_KERNEL_SMALL, stream);

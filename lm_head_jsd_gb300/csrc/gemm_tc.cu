@@ -1,6 +1,6 @@
-// Tensor-core GEMM, host side: operand tensor maps, the schedule choice
-// (tile order, split-K, stored-output prefetch, staging, epilogue groups) and
-// the split-K reduction. The kernel and its design notes are in
+// Tensor-core GEMM, host side: operand tensor maps, the schedule choice (CTA
+// pairs, tile order, split-K, stored-output prefetch, staging, epilogue
+// groups) and the split-K reduction. The kernel and its design notes are in
 // gemm_tc_kernel.cuh.
 #include "gemm_tc_kernel.cuh"
 
@@ -91,13 +91,13 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int
 }
 
 // One launch in the layout of (a_mn, b_mn).
-cudaError_t launch_layout(bool a_mn, bool b_mn, const CUtensorMap& ma, const CUtensorMap& mb,
-                          const CUtensorMap& mcm, const CUtensorMap& msm, __nv_bfloat16* d,
-                          const KParams& p, cudaStream_t st) {
-  if (!a_mn && !b_mn) return launch_kk(ma, mb, mcm, msm, d, p, st);
-  if (!a_mn && b_mn) return launch_kmn(ma, mb, mcm, msm, d, p, st);
-  if (a_mn && b_mn) return launch_mnmn(ma, mb, mcm, msm, d, p, st);
-  return launch_mnk(ma, mb, mcm, msm, d, p, st);
+cudaError_t launch_layout(bool a_mn, bool b_mn, bool pair, const CUtensorMap& ma,
+                          const CUtensorMap& mb, const CUtensorMap& mcm, const CUtensorMap& msm,
+                          __nv_bfloat16* d, const KParams& p, cudaStream_t st) {
+  if (!a_mn && !b_mn) return launch_kk(ma, mb, mcm, msm, d, p, pair, st);
+  if (!a_mn && b_mn) return launch_kmn(ma, mb, mcm, msm, d, p, pair, st);
+  if (a_mn && b_mn) return launch_mnmn(ma, mb, mcm, msm, d, p, pair, st);
+  return launch_mnk(ma, mb, mcm, msm, d, p, pair, st);
 }
 
 }  // namespace
@@ -119,6 +119,23 @@ bool tc_gemm_supported(const TcGemmArgs& g) {
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   if (!tc_gemm_supported(g)) return cudaErrorInvalidValue;
   const int64_t mblocks = (g.m + BM - 1) / BM;
+  // split-K (below) for outputs with too few tiles for the GPU; otherwise
+  // pairs of m-blocks run as CTA pairs wherever there are two m-blocks to
+  // pair. FLJSD_GEMM_PAIR=0 in the environment selects one CTA per tile for
+  // every call (both schedules compute identical results).
+  const char* senv = getenv("FLJSD_GEMM_SPLITK");
+  const bool split_off = senv != nullptr && senv[0] == '0';
+  int splits = 1;
+  if (!split_off && g.splitk_ws != nullptr && !g.accumulate && g.d32 == nullptr &&
+      g.stats == nullptr) {
+    splits = splitk_factor(g.m, g.n, g.k, num_sms());
+    while (splits > 1 &&
+           (size_t)splits * (size_t)g.m * (size_t)g.ldd * sizeof(float) > g.splitk_ws_bytes)
+      --splits;
+  }
+  const char* penv_pair = getenv("FLJSD_GEMM_PAIR");
+  const bool pair_off = penv_pair != nullptr && penv_pair[0] == '0';
+  const bool pair = mblocks >= 2 && splits <= 1 && !g.single_cta && !pair_off;
   CUtensorMap ma, mb;
   bool ok;
   if (g.a_mn)  // A stored [k x m]
@@ -128,8 +145,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   if (!ok) return cudaErrorInvalidValue;
   if (g.b_mn)  // B stored [k x n]
     ok = make_map(&mb, g.b, g.n, g.k, g.ldb, 64, 64);
-  else  // B stored [n x k]
-    ok = make_map(&mb, g.b, g.k, g.n, g.ldb, BK, BN);
+  else  // B stored [n x k]; a CTA of a pair copies half the tile's rows
+    ok = make_map(&mb, g.b, g.k, g.n, g.ldb, BK, pair ? BN / 2 : BN);
   if (!ok) return cudaErrorInvalidValue;
   KParams p{};
   p.m = g.m;
@@ -142,7 +159,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   const int64_t tiles = (int64_t)p.num_m_blocks * p.num_n_blocks;
   if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
   p.num_tiles = (int)tiles;
-  p.m_units = p.num_m_blocks;
+  p.m_units = pair ? (p.num_m_blocks + 1) / 2 : p.num_m_blocks;
   p.num_units = p.m_units * p.num_n_blocks;
   p.raster = g.raster_n_fastest;
   {
@@ -154,7 +171,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
       const long mbb = strtol(b, nullptr, 10);
       if (mbb > 0 && mbb <= 4096) band_bytes = (int64_t)mbb << 20;
     }
-    const int64_t per_unit = (int64_t)BM * g.k * 2;
+    const int64_t per_unit = (int64_t)BM * (pair ? 2 : 1) * g.k * 2;
     int64_t gm = per_unit > 0 ? band_bytes / per_unit : 1;
     if (gm < 1) gm = 1;
     if (gm > p.m_units) gm = p.m_units;
@@ -175,24 +192,17 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.k_splits = 1;
   p.kb_per_split = p.num_k_blocks;
   p.partial = nullptr;
-  const char* senv = getenv("FLJSD_GEMM_SPLITK");
-  const bool split_off = senv != nullptr && senv[0] == '0';
-  if (!split_off && g.splitk_ws != nullptr && !g.accumulate && g.d32 == nullptr &&
-      g.stats == nullptr) {
-    int s_ = splitk_factor(g.m, g.n, g.k, num_sms());
-    while (s_ > 1 && (size_t)s_ * (size_t)g.m * (size_t)g.ldd * sizeof(float) > g.splitk_ws_bytes)
-      --s_;
-    if (s_ > 1) {
-      p.kb_per_split = (p.num_k_blocks + s_ - 1) / s_;
-      p.k_splits = (p.num_k_blocks + p.kb_per_split - 1) / p.kb_per_split;
-      p.partial = g.splitk_ws;
-      p.num_units = p.num_tiles * p.k_splits;
-    }
+  if (splits > 1) {
+    p.kb_per_split = (p.num_k_blocks + splits - 1) / splits;
+    p.k_splits = (p.num_k_blocks + p.kb_per_split - 1) / p.kb_per_split;
+    p.partial = g.splitk_ws;
+    p.num_units = p.num_tiles * p.k_splits;
   }
   // stored-output prefetch for an accumulating epilogue (read-modify-write of
   // D, or of the fp32 side accumulator): fewer operand stages, a slab ring for
   // the old values. FLJSD_GEMM_PREFETCH=0 in the environment turns it off.
-  p.nst = STAGES;
+  // operand stages: 4 of 48 KB on one CTA, 6 of 32 KB in a pair (192 KB)
+  p.nst = pair ? 6 : 4;
   p.nslab = 0;
   p.slab_cols = 64;
   p.cps = 2;
@@ -225,14 +235,15 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
         // stages, eight slabs and two epilogue groups (K = 128: 320 us against
         // 431 us with 3 / 5 / one group), K = 512 and 1024 with 3 / 5 / one
         // (K = 512: 514 us against 673 us), beyond that 4 / 2 / one)
+        // (a pair's stages are two thirds the size: one more of them fits)
         if (p.num_k_blocks <= 4) {
-          p.nst = 2;
+          p.nst = pair ? 3 : 2;
           p.nslab = 8;
         } else if (p.num_k_blocks <= 16) {
-          p.nst = 3;
+          p.nst = pair ? 4 : 3;
           p.nslab = 5;
         } else {
-          p.nst = 4;
+          p.nst = pair ? 6 : 4;
           p.nslab = 2;
         }
       }
@@ -261,18 +272,20 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   p.epi_groups = 1;
   if ((p.nslab == 8 && p.kb_per_split <= 4) || (p.nslab == 0 && p.kb_per_split <= 3)) {
     p.epi_groups = 2;
-    if (p.stage_out) p.nst = 3;  // room for 8 warps x 2 staging buffers
+    if (p.stage_out) p.nst = pair ? 5 : 3;  // room for 8 warps x 2 staging buffers
   }
   p.epi_mode = p.stage_out ? EPI_STAGE
                            : (p.slab_store && !p.slab_f32 ? EPI_SLAB16 : EPI_GENERIC);
+  if (smem_bytes(p.nst, p.nslab, p.stage_out ? 4 * p.epi_groups * p.nbuf : 0, pair) > SMEM_MAX)
+    return cudaErrorInvalidConfiguration;  // a schedule above would not fit (never expected)
   if (p.k_splits > 1) {
-    cudaError_t e = launch_layout(g.a_mn, g.b_mn, ma, mb, mcm, msm, d, p, st);
+    cudaError_t e = launch_layout(g.a_mn, g.b_mn, false, ma, mb, mcm, msm, d, p, st);
     if (e != cudaSuccess) return e;
     k_splitk_reduce<<<num_sms() * 4, 256, 0, st>>>(p.partial, p.k_splits, g.m, g.n, g.ldd, d);
     count_extra_launch();
     return cudaGetLastError();
   }
-  return launch_layout(g.a_mn, g.b_mn, ma, mb, mcm, msm, d, p, st);
+  return launch_layout(g.a_mn, g.b_mn, pair, ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace fljsd

@@ -45,6 +45,9 @@ struct TcGemmArgs {
   // tc_splitk_bytes(m, n, k, ...) bytes, 16-byte aligned.
   float* splitk_ws;
   size_t splitk_ws_bytes;
+  // 1: one CTA per 128 x 256 tile even where a CTA pair could take a
+  // 256 x 256 tile (the results are identical either way)
+  int single_cta = 0;
 };
 
 constexpr int TC_STATS_COLS = 128;  // columns per pass-1 partial

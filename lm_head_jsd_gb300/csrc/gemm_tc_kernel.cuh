@@ -31,6 +31,16 @@
 // (both K-major), grad_input = dZ . W (B MN-major), grad_weight = dZ^T . X
 // (both MN-major).
 //
+// CTA pairs: two CTAs of a 2-CTA cluster compute a 256 x 256 tile together
+// with tcgen05.mma.cta_group::2. Each CTA copies its own 128 rows of A and its
+// own 128 rows (half) of the B tile into its own shared memory; the MMA of the
+// leader CTA reads both CTAs' halves, so each SM pulls 32 KB per 64-deep
+// k-block from L2 instead of 48 KB. Both CTAs' copies complete on the
+// leader's stage barrier, the leader's MMA thread issues for both and each
+// CTA drains its own 128 accumulator rows from its own tensor memory. The
+// leader hands each freed stage and each finished accumulator to the other
+// CTA with a plain remote mbarrier arrive; every copy has one destination.
+//
 // Tile orders: bands of m-blocks sweeping all n-blocks (the band of A stays in
 // L2 while B streams), or n-blocks fastest.
 //
@@ -57,29 +67,39 @@ namespace tcgemm {
 
 
 constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
-constexpr int STAGES = 4;  // operand stages (at most; see KParams::nst)
+constexpr int STAGES = 6;  // operand stages (at most; see KParams::nst)
 constexpr int MAX_SLABS = 8;                    // prefetched slabs of the stored output
 constexpr int SLAB_BYTES = BM * 128;            // 128 rows x 128 bytes (64 bf16 / 32 fp32)
 constexpr int OUT_BUF_BYTES = 32 * 128;  // one warp's staging buffer: 32 rows x 128 B
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int ACC_COLS = BN;                    // fp32 accumulator columns per tile
 constexpr int TMEM_COLS = 2 * ACC_COLS;         // double-buffered accumulator
 constexpr int EPI_STAGE = 0, EPI_SLAB16 = 1, EPI_GENERIC = 2;
+constexpr int CTRL_BYTES = 512;
+
+// One operand stage of a CTA: the A tile (128 rows) and the B tile (256 rows),
+// or in a CTA pair (see the kernel) the CTA's half of the B tile (128 rows).
+__host__ __device__ constexpr int stage_bytes(bool pair) {
+  return A_BYTES + (pair ? B_BYTES / 2 : B_BYTES);
+}
 
 // 7 warps (roles at the kernel), 11 with the second epilogue group
 __host__ __device__ constexpr int threads_for(int groups) { return groups == 2 ? 352 : 224; }
 constexpr int SMEM_MAX = 232448;  // opt-in shared memory per CTA on sm_103
 // operand stages + slab ring + alignment slack + control block
 // bufs: staging buffers of all epilogue warps together (0 without stage_out)
-__host__ __device__ constexpr int smem_bytes(int nst, int nslab, int bufs) {
-  return nst * STAGE_BYTES + nslab * SLAB_BYTES + bufs * OUT_BUF_BYTES + 1024 + 256;
+__host__ __device__ constexpr int smem_bytes(int nst, int nslab, int bufs, bool pair) {
+  return nst * stage_bytes(pair) + nslab * SLAB_BYTES + bufs * OUT_BUF_BYTES + 1024 + CTRL_BYTES;
 }
-static_assert(smem_bytes(2, 8, 0) <= SMEM_MAX && smem_bytes(3, 5, 0) <= SMEM_MAX &&
-                  smem_bytes(4, 2, 0) <= SMEM_MAX && smem_bytes(4, 2, 0) <= SMEM_MAX &&
-                  smem_bytes(4, 0, 8) <= SMEM_MAX && smem_bytes(3, 0, 16) <= SMEM_MAX,
+static_assert(smem_bytes(2, 8, 0, false) <= SMEM_MAX && smem_bytes(3, 5, 0, false) <= SMEM_MAX &&
+                  smem_bytes(4, 2, 0, false) <= SMEM_MAX && smem_bytes(4, 0, 8, false) <= SMEM_MAX &&
+                  smem_bytes(3, 0, 16, false) <= SMEM_MAX,
               "shared memory");
+static_assert(smem_bytes(6, 0, 8, true) <= SMEM_MAX && smem_bytes(5, 0, 16, true) <= SMEM_MAX &&
+                  smem_bytes(4, 5, 0, true) <= SMEM_MAX && smem_bytes(6, 2, 0, true) <= SMEM_MAX &&
+                  smem_bytes(3, 8, 0, true) <= SMEM_MAX,
+              "shared memory (pairs)");
 constexpr unsigned long long kTimeoutNs = 10ull * 1000 * 1000 * 1000;  // 10 s by default
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -101,19 +121,59 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// CL: acquire at cluster scope (the phase completes through release arrivals
+// of threads in the other CTA of a pair).
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if (CL)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok != 0;
 }
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive (release, cluster scope) on an mbarrier of another CTA of the
+// cluster, given its shared::cluster address (map_to_cta).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// The same without release semantics, for hand-overs that order only
+// asynchronous work (the MMAs' reads of a stage before the next copies into
+// it).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
-// Shared-memory control block.
+// Shared-memory control block (barrier use per CTA of a pair in the kernel).
 struct Ctrl {
   unsigned long long full[STAGES];
   unsigned long long empty[STAGES];
@@ -126,15 +186,16 @@ struct Ctrl {
   uint32_t tmem_base;
   volatile int abort;
 };
-static_assert(sizeof(Ctrl) <= 256, "control block");
+static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block");
 
 // Bounded wait: true when the phase completed, false on timeout or abort
 // (then the abort flag is set and the status word records the timeout).
+template <bool CL = false>
 __device__ __forceinline__ bool wait_bar(Ctrl* cb, uint32_t bar, uint32_t parity, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<CL>(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CL>(bar, parity)) return true;
     if ((it & 63u) == 63u) {
       if (cb->abort) return false;
       if (globaltimer() - t0 > cb->timeout_ns) {
@@ -155,6 +216,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The copy of a CTA pair: lands in this CTA's shared memory and completes
+// (complete_tx) on the mbarrier at shared::cluster address `bar`, which may be
+// the other CTA's (the leader's).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
 // Shared -> global tensor copy (clipped at the tensor's bounds), tracked by
 // bulk groups of the issuing thread.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
@@ -209,24 +281,65 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 
 // Instruction descriptor, kind::f16: D fp32 ([4,6) = 1), A and B bf16
 // ([7,10) = 1, [10,13) = 1), A / B major ([15], [16]: 1 = MN-major),
-// N >> 3 at [17,23), M >> 4 at [24,29).
-__host__ __device__ constexpr uint32_t instr_desc(bool a_mn, bool b_mn) {
+// N >> 3 at [17,23), M >> 4 at [24,29). M is 128 on one CTA and 256 on a CTA
+// pair (128 rows in each CTA's tensor memory).
+__host__ __device__ constexpr uint32_t instr_desc(bool a_mn, bool b_mn, bool pair) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)((pair ? 2 * BM : BM) >> 4) << 24);
 }
 
+// tcgen05 instructions of one kernel all name the same CTA group: ::1 for one
+// CTA per tile, ::2 for a CTA pair.
+template <bool PAIR>
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+  if (PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
+// Arrive on this CTA's mbarrier `bar` once every MMA this thread issued has
+// completed (for a pair: in both CTAs).
+template <bool PAIR>
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
+  if (PAIR)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// Tensor-memory allocation: one warp per CTA (for a pair, one warp in each CTA,
+// together).
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t cols) {
+  if (PAIR) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(cols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(cols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  if (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols));
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols));
 }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -273,7 +386,8 @@ struct KParams {
   float2* stats;       // [m x num_n_blocks] (max, sum 2^(x - max)) per row and tile, or null
   float stats_scale;   // x = bf16(value) * stats_scale
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
-  // scheduling units: m-blocks (one CTA per tile)
+  // scheduling units: m-blocks (one CTA per tile) or pairs of m-blocks (a CTA
+  // pair per 256 x 256 tile)
   int m_units, num_units;
   int raster;   // 0: bands of group_m m-units sweeping all n-blocks; 1: n-blocks fastest
   int group_m;  // m-units per band
@@ -442,19 +556,35 @@ static __device__ __noinline__ void store_chunk_generic(const KParams& p, float*
   }
 }
 
-template <bool A_MN, bool B_MN, int G, int EPI>
+// Barrier use (one CTA per tile | CTA pair: leader, i.e. cluster rank 0 | other CTA):
+//   full[s]        copies of stage s landed | both CTAs' copies (the leader
+//                  expects the bytes of both) | unused
+//   empty[s]       the MMA read stage s | same | the leader handed stage s on (remote
+//                  arrive, once per fill, after expecting both CTAs' bytes)
+//   tmem_full[a]   accumulator a complete | same | relayed by the leader's epilogue
+//   tmem_empty[a]  4G epilogue warps drained accumulator a | 4G warps of each CTA | unused
+// Stage data moves only through the asynchronous proxy (TMA writes, MMA
+// reads), ordered by the barriers' transaction counts and tcgen05.commit, so
+// the stage waits are CTA-scoped and the leader hands a stage on with a
+// relaxed remote arrive (a release at cluster scope cost ~0.5 us per fill and
+// halved the pair's throughput, measured). The accumulator hand-offs, once
+// per tile, release and acquire at cluster scope.
+template <bool A_MN, bool B_MN, bool PAIR, int G, int EPI>
 __global__ void __launch_bounds__(threads_for(G), 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
               __nv_bfloat16* __restrict__ D, KParams p) {
+  constexpr int SB = stage_bytes(PAIR);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t cslabs = base + p.nst * STAGE_BYTES;  // slab ring (1024-aligned)
-  uint8_t* stg = gbase + p.nst * STAGE_BYTES + p.nslab * SLAB_BYTES;  // output staging
+  const uint32_t cslabs = base + p.nst * SB;  // slab ring (1024-aligned)
+  uint8_t* stg = gbase + p.nst * SB + p.nslab * SLAB_BYTES;  // output staging
   Ctrl* cb = reinterpret_cast<Ctrl*>(stg + (p.stage_out ? 4 * G * p.nbuf * OUT_BUF_BYTES : 0));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -463,7 +593,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&cb->tmem_full[a]), 1);
-      mbar_init(smem_u32(&cb->tmem_empty[a]), 4 * G);
+      mbar_init(smem_u32(&cb->tmem_empty[a]), PAIR ? 8 * G : 4 * G);
     }
     for (int s = 0; s < MAX_SLABS; ++s) {
       mbar_init(smem_u32(&cb->cfull[s]), 1);
@@ -479,18 +609,16 @@ __global__ void __launch_bounds__(threads_for(G), 1)
     if (p.nslab > 0) prefetch_tensormap(&tmC);
     if (p.slab_store || p.stage_out) prefetch_tensormap(&tmS);
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&cb->tmem_base)),
-                 "r"(TMEM_COLS));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
+  // the other CTA's copies and arrivals target this CTA's barriers: they must
+  // be initialised cluster-wide before anyone issues
+  if (PAIR) cluster_sync_all();
+  if (warp == 1) tmem_alloc<PAIR>(smem_u32(&cb->tmem_base), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = cb->tmem_base;
-  const int unit0 = (int)blockIdx.x;
-  const int unit_step = (int)gridDim.x;
+  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int unit_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   // Tile order. n-fastest: all n-blocks of a few m-blocks run together (used
   // when B is small and A streams). Grouped: bands of group_m m-blocks; inside
@@ -509,7 +637,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
       mu = m0 + r % gm;
       nb = r / gm;
     }
-    mb = mu;
+    mb = PAIR ? 2 * mu + (int)rank : mu;
   };
   auto unit_split = [&](int t, int& tile, int& split, int& kb0, int& kb1) {
     if (p.k_splits > 1) {
@@ -534,32 +662,61 @@ __global__ void __launch_bounds__(threads_for(G), 1)
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false;
       bool ok = !p.stall_producer;
+      // A pair's other CTA fills a stage only when the leader hands it on:
+      // the k-th hand-over of stage s completes phase k of its empty[s], so
+      // it waits for the parity of the current round, where the leader (and
+      // a single CTA) waits for the MMA to have released the previous round.
+      const uint32_t flip = (PAIR && !leader) ? 0u : 1u;
       for (int t = unit0; ok && t < p.num_units; t += unit_step) {
         int mb, nb, tile, split, kb0, kb1;
         unit_split(t, tile, split, kb0, kb1);
         tile_coords(tile, mb, nb);
         const int m0 = mb * BM, n0 = nb * BN;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_bar(cb, smem_u32(&cb->empty[stage]), phase ^ 1u, p.status)) {
+          if (!wait_bar(cb, smem_u32(&cb->empty[stage]), phase ^ flip, p.status)) {
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(&cb->full[stage]);
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          const uint32_t sa = base + stage * STAGE_BYTES;
+          const uint32_t sa = base + stage * SB;
           const uint32_t sb = sa + A_BYTES;
           const int k0 = kb * BK;
-          if (A_MN) {
-            tma_load_2d(sa, &tmA, fb, m0, k0);
-            tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, k0);
+          if (PAIR) {
+            // both CTAs' copies complete on the leader's barrier, which
+            // expects the bytes of both before the other CTA may copy (the
+            // MMA has read both halves of the previous round by now)
+            const uint32_t fb = map_to_cta(smem_u32(&cb->full[stage]), 0);
+            if (leader) {
+              mbar_arrive_expect_tx(smem_u32(&cb->full[stage]), 2 * SB);
+              mbar_arrive_remote_relaxed(map_to_cta(smem_u32(&cb->empty[stage]), 1));
+            }
+            if (A_MN) {
+              tma_load_2d_pair(sa, &tmA, fb, m0, k0);
+              tma_load_2d_pair(sa + 8192, &tmA, fb, m0 + 64, k0);
+            } else {
+              tma_load_2d_pair(sa, &tmA, fb, k0, m0);
+            }
+            const int nh = n0 + (int)rank * (BN / 2);  // this CTA's half of the B tile
+            if (B_MN) {
+              tma_load_2d_pair(sb, &tmB, fb, nh, k0);
+              tma_load_2d_pair(sb + 8192, &tmB, fb, nh + 64, k0);
+            } else {
+              tma_load_2d_pair(sb, &tmB, fb, k0, nh);
+            }
           } else {
-            tma_load_2d(sa, &tmA, fb, k0, m0);
-          }
-          if (B_MN) {
+            const uint32_t fb = smem_u32(&cb->full[stage]);
+            mbar_arrive_expect_tx(fb, SB);
+            if (A_MN) {
+              tma_load_2d(sa, &tmA, fb, m0, k0);
+              tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, k0);
+            } else {
+              tma_load_2d(sa, &tmA, fb, k0, m0);
+            }
+            if (B_MN) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tmB, fb, n0 + 64 * j, k0);
-          } else {
-            tma_load_2d(sb, &tmB, fb, k0, n0);
+              for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tmB, fb, n0 + 64 * j, k0);
+            } else {
+              tma_load_2d(sb, &tmB, fb, k0, n0);
+            }
           }
           issued[stage] = true;
           issued_parity[stage] = phase;
@@ -569,14 +726,19 @@ __global__ void __launch_bounds__(threads_for(G), 1)
           }
         }
       }
-      // drain: every issued copy has landed before the CTA may exit
-      for (int s = 0; s < STAGES; ++s)
-        if (issued[s]) wait_bar(cb, smem_u32(&cb->full[s]), issued_parity[s], p.status);
+      // drain: every issued copy has landed before the CTA may exit. A pair's
+      // leader waits for both CTAs' copies (they complete on its barriers;
+      // the other CTA copies into a stage only after the leader has expected
+      // its bytes), and the cluster barrier at the exit keeps the other CTA
+      // resident until then.
+      if (!PAIR || leader)
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) wait_bar(cb, smem_u32(&cb->full[s]), issued_parity[s], p.status);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = instr_desc(A_MN, B_MN);
+    // ---------------- MMA issuer (a pair's leader issues for both CTAs) ----------------
+    if (lane == 0 && (!PAIR || leader)) {
+      constexpr uint32_t idesc = instr_desc(A_MN, B_MN, PAIR);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -585,7 +747,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
       for (int t = unit0; ok && t < p.num_units; t += unit_step, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        if (!wait_bar(cb, smem_u32(&cb->tmem_empty[acc]), acc_phase ^ 1u, p.status)) break;
+        if (!wait_bar<PAIR>(cb, smem_u32(&cb->tmem_empty[acc]), acc_phase ^ 1u, p.status)) break;
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + acc * ACC_COLS;
         int tile_i, split_i, kb0, kb1;
@@ -596,7 +758,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = base + stage * STAGE_BYTES;
+          const uint32_t sa = base + stage * SB;
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
@@ -609,10 +771,10 @@ __global__ void __launch_bounds__(threads_for(G), 1)
               bd = smem_desc(sb + kk * (UMMA_K * 128), 8192, 1024);
             else
               bd = smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
-            mma_bf16(tmem_d, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            mma_bf16<PAIR>(tmem_d, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          // frees the stage once read
-          mma_commit(smem_u32(&cb->empty[stage]));
+          // frees the stage once read (in a pair: both CTAs' halves)
+          mma_commit<PAIR>(smem_u32(&cb->empty[stage]));
           any = true;
           if (++stage == p.nst) {
             stage = 0;
@@ -620,11 +782,11 @@ __global__ void __launch_bounds__(threads_for(G), 1)
           }
         }
         if (!ok) break;
-        mma_commit(smem_u32(&cb->tmem_full[acc]));
+        mma_commit<PAIR>(smem_u32(&cb->tmem_full[acc]));
       }
       if (any) {
         // all issued MMAs have completed before tensor memory is released
-        mma_commit(smem_u32(&cb->drain));
+        mma_commit<PAIR>(smem_u32(&cb->drain));
         wait_bar(cb, smem_u32(&cb->drain), 0, p.status);
       }
     }
@@ -692,7 +854,13 @@ __global__ void __launch_bounds__(threads_for(G), 1)
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       bool ok = true;
-      if (lane == 0) ok = wait_bar(cb, smem_u32(&cb->tmem_full[acc]), acc_phase, p.status);
+      if (lane == 0) {
+        ok = wait_bar<PAIR>(cb, smem_u32(&cb->tmem_full[acc]), acc_phase, p.status);
+        // the leader's first epilogue warp tells the other CTA that its rows
+        // of the accumulator are complete too (the MMAs were issued here)
+        if (PAIR && ok && leader && ew == 0)
+          mbar_arrive_remote(map_to_cta(smem_u32(&cb->tmem_full[acc]), 1));
+      }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
@@ -729,7 +897,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
               break;
             }
           }
-          crow = gbase + p.nst * STAGE_BYTES + cslot * SLAB_BYTES + (sub * 32 + lane) * 128;
+          crow = gbase + p.nst * SB + cslot * SLAB_BYTES + (sub * 32 + lane) * 128;
         }
         if (kStage && (c & 1) == 0) {
           // the store that last used this staging buffer has read it
@@ -878,7 +1046,14 @@ __global__ void __launch_bounds__(threads_for(G), 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&cb->tmem_empty[acc]));
+      if (lane == 0) {
+        // the accumulator's MMAs are the leader's: its barrier counts the
+        // epilogue warps of both CTAs
+        if (PAIR && !leader)
+          mbar_arrive_remote(map_to_cta(smem_u32(&cb->tmem_empty[acc]), 0));
+        else
+          mbar_arrive(smem_u32(&cb->tmem_empty[acc]));
+      }
     }
     if ((kSlabStore || kStage) && lane == 0) {
       // every store of this warp has completed before the CTA may exit
@@ -889,56 +1064,87 @@ __global__ void __launch_bounds__(threads_for(G), 1)
 
   tc_fence_before();
   __syncthreads();
+  // no CTA of a pair leaves while the other may still read its shared memory
+  // (the leader's MMAs), land copies on its barriers or arrive on them
+  if (PAIR) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(TMEM_COLS));
+    tmem_dealloc<PAIR>(tmem_base, TMEM_COLS);
   }
 }
 
-template <bool A_MN, bool B_MN, int G, int EPI>
+template <bool A_MN, bool B_MN, bool PAIR, int G, int EPI>
 cudaError_t launch_g(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mcm,
                      const CUtensorMap& msm, __nv_bfloat16* d, KParams p, cudaStream_t st) {
   constexpr int THREADS = threads_for(G);
-  const int smem = smem_bytes(p.nst, p.nslab, p.stage_out ? 4 * G * p.nbuf : 0);
+  const int smem = smem_bytes(p.nst, p.nslab, p.stage_out ? 4 * G * p.nbuf : 0, PAIR);
+  static int max_clusters[64] = {0};
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   const bool cache = dev >= 0 && dev < 64;
-  auto kern = k_gemm_tc<A_MN, B_MN, G, EPI>;
+  auto kern = k_gemm_tc<A_MN, B_MN, PAIR, G, EPI>;
   if (!cache || !attr_set[dev]) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
     if (e != cudaSuccess) return e;
     if (cache) attr_set[dev] = true;
   }
-  const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
-  kern<<<grid, THREADS, smem, st>>>(ma, mb, mcm, msm, d, p);
+  if (!PAIR) {
+    const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
+    kern<<<grid, THREADS, smem, st>>>(ma, mb, mcm, msm, d, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // a persistent grid must not exceed the clusters that can be resident at once
+  if (!cache || max_clusters[dev] == 0) {
+    int n = 0;
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = 1;
+    if (cache) max_clusters[dev] = n;
+    else max_clusters[0] = n;
+  }
+  const int mc = cache ? max_clusters[dev] : max_clusters[0];
+  const int clusters = p.num_units < mc ? p.num_units : mc;
+  cfg.gridDim = dim3(2 * clusters);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mcm, msm, d, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-// Every (epilogue groups, epilogue mode) variant of one layout.
-template <bool A_MN, bool B_MN>
+// Every (epilogue groups, epilogue mode) variant of one layout and schedule.
+template <bool A_MN, bool B_MN, bool PAIR>
 cudaError_t launch_modes(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mcm,
                          const CUtensorMap& msm, __nv_bfloat16* d, const KParams& p,
                          cudaStream_t st) {
   if (p.epi_groups == 2) {
-    if (p.epi_mode == EPI_STAGE) return launch_g<A_MN, B_MN, 2, EPI_STAGE>(ma, mb, mcm, msm, d, p, st);
-    if (p.epi_mode == EPI_SLAB16) return launch_g<A_MN, B_MN, 2, EPI_SLAB16>(ma, mb, mcm, msm, d, p, st);
-    return launch_g<A_MN, B_MN, 2, EPI_GENERIC>(ma, mb, mcm, msm, d, p, st);
+    if (p.epi_mode == EPI_STAGE) return launch_g<A_MN, B_MN, PAIR, 2, EPI_STAGE>(ma, mb, mcm, msm, d, p, st);
+    if (p.epi_mode == EPI_SLAB16) return launch_g<A_MN, B_MN, PAIR, 2, EPI_SLAB16>(ma, mb, mcm, msm, d, p, st);
+    return launch_g<A_MN, B_MN, PAIR, 2, EPI_GENERIC>(ma, mb, mcm, msm, d, p, st);
   }
-  if (p.epi_mode == EPI_STAGE) return launch_g<A_MN, B_MN, 1, EPI_STAGE>(ma, mb, mcm, msm, d, p, st);
-  if (p.epi_mode == EPI_SLAB16) return launch_g<A_MN, B_MN, 1, EPI_SLAB16>(ma, mb, mcm, msm, d, p, st);
-  return launch_g<A_MN, B_MN, 1, EPI_GENERIC>(ma, mb, mcm, msm, d, p, st);
+  if (p.epi_mode == EPI_STAGE) return launch_g<A_MN, B_MN, PAIR, 1, EPI_STAGE>(ma, mb, mcm, msm, d, p, st);
+  if (p.epi_mode == EPI_SLAB16) return launch_g<A_MN, B_MN, PAIR, 1, EPI_SLAB16>(ma, mb, mcm, msm, d, p, st);
+  return launch_g<A_MN, B_MN, PAIR, 1, EPI_GENERIC>(ma, mb, mcm, msm, d, p, st);
 }
 
 // Launchers of one operand layout (A K-major or MN-major, B likewise), each
-// defined in its own translation unit: every epilogue variant (one or two
-// epilogue groups, from p.epi_groups).
+// defined in its own translation unit: every schedule (CTA pairs or one CTA
+// per tile) and epilogue variant (one or two epilogue groups, from
+// p.epi_groups).
 #define FLJSD_TC_LAUNCHER(name)                                                    \
   cudaError_t name(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mcm, \
-                   const CUtensorMap& msm, __nv_bfloat16* d, const KParams& p,    \
+                   const CUtensorMap& msm, __nv_bfloat16* d, const KParams& p, bool pair, \
                    cudaStream_t st)
 FLJSD_TC_LAUNCHER(launch_kk);
 FLJSD_TC_LAUNCHER(launch_kmn);

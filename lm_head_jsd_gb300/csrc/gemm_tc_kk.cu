@@ -5,7 +5,8 @@ namespace fljsd {
 namespace tcgemm {
 
 FLJSD_TC_LAUNCHER(launch_kk) {
-  return launch_modes<false, false>(ma, mb, mcm, msm, d, p, st);
+  return pair ? launch_modes<false, false, true>(ma, mb, mcm, msm, d, p, st)
+              : launch_modes<false, false, false>(ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace tcgemm

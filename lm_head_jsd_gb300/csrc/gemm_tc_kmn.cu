@@ -5,7 +5,8 @@ namespace fljsd {
 namespace tcgemm {
 
 FLJSD_TC_LAUNCHER(launch_kmn) {
-  return launch_modes<false, true>(ma, mb, mcm, msm, d, p, st);
+  return pair ? launch_modes<false, true, true>(ma, mb, mcm, msm, d, p, st)
+              : launch_modes<false, true, false>(ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace tcgemm

@@ -5,7 +5,8 @@ namespace fljsd {
 namespace tcgemm {
 
 FLJSD_TC_LAUNCHER(launch_mnk) {
-  return launch_modes<true, false>(ma, mb, mcm, msm, d, p, st);
+  return pair ? launch_modes<true, false, true>(ma, mb, mcm, msm, d, p, st)
+              : launch_modes<true, false, false>(ma, mb, mcm, msm, d, p, st);
 }
 
 }  // namespace tcgemm

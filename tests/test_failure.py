@@ -10,9 +10,12 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("acc", [0, 1], ids=["store", "accumulate"])
-def test_gemm_wait_timeout_is_reported_and_the_context_survives(acc):
+@pytest.mark.parametrize("pairs", [True, False], ids=["pairs", "single"])
+def test_gemm_wait_timeout_is_reported_and_the_context_survives(pairs, acc):
     """With acc = 1 the stored output is read ahead by the prefetch warp, whose
-    ring of slabs fills and whose waits then expire as well."""
+    ring of slabs fills and whose waits then expire as well. In a CTA pair
+    both CTAs' waits expire (each on its own clock) and both leave through
+    the cluster barrier at the exit."""
     from lm_head_jsd_gb300 import _lib
 
     m, n, k = 512, 512, 256
@@ -22,14 +25,15 @@ def test_gemm_wait_timeout_is_reported_and_the_context_survives(acc):
     d0 = torch.randn(m, n, generator=g, device="cuda").to(torch.bfloat16)
     d = d0.clone()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    flags = _lib.FLJSD_GEMM_TEST_STALL
+    flags = _lib.FLJSD_GEMM_TEST_STALL | (0 if pairs else _lib.FLJSD_GEMM_SINGLE_CTA)
     _lib.fljsd_gemm_bf16(a, k, 0, b, k, 0, d, n, m, n, k, acc, status, flags)
     torch.cuda.synchronize()
     assert status.item() == 5  # FLJSD_ERR_TIMEOUT
     # the same GEMM, unstalled, on the same context
     d.copy_(d0)
     status.zero_()
-    _lib.fljsd_gemm_bf16(a, k, 0, b, k, 0, d, n, m, n, k, acc, status, 0)
+    _lib.fljsd_gemm_bf16(a, k, 0, b, k, 0, d, n, m, n, k, acc, status,
+                         0 if pairs else _lib.FLJSD_GEMM_SINGLE_CTA)
     torch.cuda.synchronize()
     assert status.item() == 0
     ref = a.float() @ b.float().t() + (d0.float() if acc else 0.0)

@@ -98,3 +98,64 @@ def test_full_size(name, chunk):
     mask = torch.ones(w.bt, dtype=torch.bool)
     mask[R] = False
     assert int(torch.count_nonzero(giC[mask.to(dev)])) == 0
+
+
+GOLDEN = __import__("os").path.join(__import__("os").path.dirname(__file__), "golden",
+                                     "llama3_lmhead_golden.npz")
+
+
+@pytest.fixture(scope="module")
+def llama3_cpu_inputs():
+    """The Llama-3-8B lm_head workload drawn on the CPU (the draw the stored
+    oracle values were computed from), with the digests of its tensors."""
+    import hashlib
+
+    w = jsd_inputs.WORKLOADS["llama3_lmhead"]
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    names = ("x_s", "w_s", "x_t", "w_t", "labels")
+    digests = {n: hashlib.sha256(t.contiguous().view(-1).view(torch.uint8).numpy().tobytes())
+               .hexdigest() for n, t in zip(names, inputs)}
+    return w, inputs, digests
+
+
+@pytest.mark.parametrize("chunk", [4096, 512, 128])
+def test_full_size_against_stored_oracle(llama3_cpu_inputs, chunk):
+    """The benchmarked launch of the Llama-3-8B lm_head shape (BT=4096,
+    H=4096, V=128256, bf16, 5% ignored rows) over every row, against float64
+    oracle values stored by tests/golden/make_llama3_lmhead_golden.py: the
+    batchmean loss, the per-row losses, 64 grad_weight rows (first and last
+    vocabulary ids, the last 256-column tile, 128-column boundaries, random
+    ids) and 8 grad_input rows (one of them an ignored row: exactly 0). At
+    chunk rows 128 each of the 32 chunks adds its product into the stored bf16
+    grad_weight (PR 1429 "Summary": first chunk overwrites, later chunks add
+    in fp32 and round once)."""
+    w, inputs, digests = llama3_cpu_inputs
+    g = np.load(GOLDEN)
+    for n, d in digests.items():
+        assert str(g[f"sha256_{n}"]) == d, f"input {n} differs from the stored oracle's draw"
+    dev = "cuda:0"
+    x_s, w_s, x_t, w_t, labels = (t.to(dev) for t in inputs)
+    tol_loss, tol_grad = TOL[w.dtype]
+    loss, gi, gw = run_gpu(x_s, w_s, x_t, w_t, labels, beta=w.beta, temperature=w.temperature,
+                           reduction=w.reduction, chunk_rows=chunk)
+    ref_loss = float(g["loss"])
+    e = abs(loss.item() - ref_loss) / abs(ref_loss)
+    assert e <= tol_loss, f"loss {loss.item()} vs {ref_loss}: {e:.3g}"
+    J = torch.from_numpy(g["vocab_ids"]).to(dev)
+    e = rel_fro(f64(gw[J]), g["grad_weight_rows"].astype(np.float64))
+    assert e <= tol_grad, f"grad_weight rows: {e:.3g}"
+    R = g["row_ids"]
+    gi_R = f64(gi[torch.from_numpy(R).to(dev)])
+    ref_gi = g["grad_input_rows"].astype(np.float64)
+    e = rel_fro(gi_R, ref_gi)
+    assert e <= tol_grad, f"grad_input rows: {e:.3g}"
+    ignored = labels.cpu().numpy()[R] == -100
+    assert ignored.any() and np.all(gi_R[ignored] == 0.0)
+    del gi, gw
+    if chunk == 4096:
+        rows, _, _ = run_gpu(x_s, w_s, x_t, w_t, labels, beta=w.beta, temperature=w.temperature,
+                             reduction="none", chunk_rows=chunk)
+        e = rel_fro(f64(rows), g["loss_rows"])
+        assert e <= tol_loss, f"per-row losses: {e:.3g}"
+        assert np.all(f64(rows)[labels.cpu().numpy() == -100] == 0.0)
+    torch.cuda.empty_cache()

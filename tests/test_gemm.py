@@ -29,10 +29,10 @@ def _ref(a, a_mn, b, b_mn):
     return A @ B.t()
 
 
+@pytest.mark.parametrize("flags", [0, 1], ids=["pairs", "single"])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_gemm_layouts(a_mn, b_mn, shape):
-    flags = 0
+def test_gemm_layouts(a_mn, b_mn, shape, flags):
     from lm_head_jsd_gb300 import fljsd_gemm_bf16
 
     m, n, k = shape
@@ -86,12 +86,40 @@ def test_gemm_rejects_bad_arguments():
     assert fljsd_gemm_bf16(a, 16, 0, a, 16, 0, a, 16, 16, 16, 16, flags=4, check=False) == 1
 
 
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
+@pytest.mark.parametrize("shape", [(1000, 777, 300), (256, 512, 64), (384, 1000, 1000),
+                                   (4096, 4096, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_gemm_pairs_and_single_ctas_agree_bitwise(a_mn, b_mn, shape):
+    """A CTA pair computes a 256-row tile with one MMA instruction over both
+    CTAs' shared memory; one CTA computes 128 rows. The products and their
+    fp32 accumulation order are the same, so both schedules give identical
+    bits (including an odd m-block count, whose last pair has an empty half)."""
+    from lm_head_jsd_gb300 import fljsd_gemm_bf16
+
+    m, n, k = shape
+    g = torch.Generator(device="cuda").manual_seed(11 + m + n + k)
+    a, lda = _operand(a_mn, k if a_mn else m, m if a_mn else k, g)
+    b, ldb = _operand(b_mn, k if b_mn else n, n if b_mn else k, g)
+    ldd = -(-n // 8) * 8
+    d0 = torch.empty(m, ldd, dtype=torch.bfloat16, device="cuda")
+    d1 = torch.empty(m, ldd, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d0, ldd, m, n, k, 0, status, 0)
+    fljsd_gemm_bf16(a, lda, a_mn, b, ldb, b_mn, d1, ldd, m, n, k, 0, status, 1)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(d0[:, :n], d1[:, :n])
+    ref = _ref(a, a_mn, b, b_mn)
+    assert ((d0[:, :n].float() - ref).norm() / ref.norm()).item() < 4e-3
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["pairs", "single"])
 @pytest.mark.parametrize("a_mn,b_mn", [(1, 1), (0, 0), (0, 1)])
 @pytest.mark.parametrize("shape", [(1000, 777, 128), (300, 1000, 640), (129, 4096, 2048),
                                    (5000, 4096, 64)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_gemm_accumulate_prefetch_matches_plain_loads(a_mn, b_mn, shape, monkeypatch):
-    flags = 0
+def test_gemm_accumulate_prefetch_matches_plain_loads(a_mn, b_mn, shape, flags, monkeypatch):
     """The accumulating epilogue reads the old values from slabs copied ahead by
     TMA (shallow, middle and deep operand rings by contraction length); with the
     copy turned off it reads them with plain loads. Same arithmetic, so the
@@ -121,11 +149,11 @@ def test_gemm_accumulate_prefetch_matches_plain_loads(a_mn, b_mn, shape, monkeyp
     assert err < 4e-3, float(err)
 
 
+@pytest.mark.parametrize("flags", [0, 1], ids=["pairs", "single"])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
 @pytest.mark.parametrize("shape", [(1000, 1000, 128), (129, 4096, 640), (300, 264, 4096)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_gemm_staged_output_matches_plain_stores(a_mn, b_mn, shape, monkeypatch):
-    flags = 0
+def test_gemm_staged_output_matches_plain_stores(a_mn, b_mn, shape, flags, monkeypatch):
     """A plain (non-accumulating) bf16 output goes through shared-memory staging
     buffers and TMA stores; with staging turned off each thread stores its row.
     Same rounding, so the results agree bitwise; the stores are clipped at the
