@@ -75,6 +75,9 @@ WORKLOADS = {
     # traffic per launch scale with V, so profiler counters taken here scale
     # to the headline by 4
     "headline_v32k": Workload("headline_v32k", 8, 8192, 4096, 4096, 32064, "bf16"),
+    # the headline's V with a small H and BT (about 1.5 GB on the device): the
+    # row kernel, which does not depend on H, at full row length
+    "rows_v128k": Workload("rows_v128k", 9, 2048, 512, 512, 128256, "bf16"),
 }
 
 

@@ -215,17 +215,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-
-// The copy of a CTA pair: lands in this CTA's shared memory and completes
-// (complete_tx) on the mbarrier at shared::cluster address `bar`, which may be
-// the other CTA's (the leader's).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar, int32_t x, int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
+// Operand copies. In a CTA pair (PAIR) the copy lands in this CTA's shared
+// memory and completes (complete_tx) on the mbarrier at shared::cluster
+// address `bar`, which may be the other CTA's (the leader's).
+template <bool PAIR>
+__device__ __forceinline__ void tma_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+  if (PAIR)
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+  else
+    tma_load_2d(dst, map, bar, x, y);
 }
 // Shared -> global tensor copy (clipped at the tensor's bounds), tracked by
 // bulk groups of the issuing thread.
@@ -680,43 +683,36 @@ __global__ void __launch_bounds__(threads_for(G), 1)
           const uint32_t sa = base + stage * SB;
           const uint32_t sb = sa + A_BYTES;
           const int k0 = kb * BK;
+          uint32_t fb;
+          int nh, nb_rows;  // this CTA's rows of the B tile
           if (PAIR) {
             // both CTAs' copies complete on the leader's barrier, which
             // expects the bytes of both before the other CTA may copy (the
             // MMA has read both halves of the previous round by now)
-            const uint32_t fb = map_to_cta(smem_u32(&cb->full[stage]), 0);
+            fb = map_to_cta(smem_u32(&cb->full[stage]), 0);
             if (leader) {
               mbar_arrive_expect_tx(smem_u32(&cb->full[stage]), 2 * SB);
               mbar_arrive_remote_relaxed(map_to_cta(smem_u32(&cb->empty[stage]), 1));
             }
-            if (A_MN) {
-              tma_load_2d_pair(sa, &tmA, fb, m0, k0);
-              tma_load_2d_pair(sa + 8192, &tmA, fb, m0 + 64, k0);
-            } else {
-              tma_load_2d_pair(sa, &tmA, fb, k0, m0);
-            }
-            const int nh = n0 + (int)rank * (BN / 2);  // this CTA's half of the B tile
-            if (B_MN) {
-              tma_load_2d_pair(sb, &tmB, fb, nh, k0);
-              tma_load_2d_pair(sb + 8192, &tmB, fb, nh + 64, k0);
-            } else {
-              tma_load_2d_pair(sb, &tmB, fb, k0, nh);
-            }
+            nh = n0 + (int)rank * (BN / 2);
+            nb_rows = BN / 2;
           } else {
-            const uint32_t fb = smem_u32(&cb->full[stage]);
+            fb = smem_u32(&cb->full[stage]);
             mbar_arrive_expect_tx(fb, SB);
-            if (A_MN) {
-              tma_load_2d(sa, &tmA, fb, m0, k0);
-              tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, k0);
-            } else {
-              tma_load_2d(sa, &tmA, fb, k0, m0);
-            }
-            if (B_MN) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tmB, fb, n0 + 64 * j, k0);
-            } else {
-              tma_load_2d(sb, &tmB, fb, k0, n0);
-            }
+            nh = n0;
+            nb_rows = BN;
+          }
+          if (A_MN) {
+            tma_operand<PAIR>(sa, &tmA, fb, m0, k0);
+            tma_operand<PAIR>(sa + 8192, &tmA, fb, m0 + 64, k0);
+          } else {
+            tma_operand<PAIR>(sa, &tmA, fb, k0, m0);
+          }
+          if (B_MN) {
+            for (int j = 0; j < nb_rows / 64; ++j)
+              tma_operand<PAIR>(sb + j * 8192, &tmB, fb, nh + 64 * j, k0);
+          } else {
+            tma_operand<PAIR>(sb, &tmB, fb, k0, nh);
           }
           issued[stage] = true;
           issued_parity[stage] = phase;

@@ -125,11 +125,11 @@ __device__ __forceinline__ void lean_terms(float zs, float zt, float c, float oa
   Q = ex2(X2);
   P = ex2(Y2);
   // M + 2^-126 instead of max(M, 2^-126): the same guard against log2(0)
-  // where both terms flush to zero, one instruction less
-  const float lM = lg2(fmaf(omb, Q, fmaf(beta, P, 1.17549435e-38f)));
-  const bool tie = X2 == Y2;
-  xm = tie ? 0.f : X2 - lM;
-  ym = tie ? 0.f : Y2 - lM;
+  // where both terms flush to zero, one instruction less. At a tie log2 M is
+  // taken as X2 (= Y2) itself, so that both log ratios are exactly 0.
+  const float lM = (X2 == Y2) ? X2 : lg2(fmaf(omb, Q, fmaf(beta, P, 1.17549435e-38f)));
+  xm = X2 - lM;
+  ym = Y2 - lM;
 }
 
 template <typename T, int BRANCH>
