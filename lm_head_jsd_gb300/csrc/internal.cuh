@@ -47,6 +47,7 @@ struct JsdRowArgs {
   float scale_log2;  // log2(e) / T, the same constant the GEMM epilogue used
   float loss_scale;  // 1, or T^2 with FLJSD_FLAG_T2 (loss and gradients)
   int64_t cache_vec; // set by the launcher: vectors of X - log M kept in shared memory
+  int rows_prefetch; // set by the launcher: L2 prefetch ahead of pass 2 (lean path)
 };
 
 cudaError_t launch_count_valid(const int64_t* labels, int64_t bt, int64_t ignore_index,

@@ -27,6 +27,7 @@ using namespace rowmath;
 constexpr int kRowThreads = 1024;
 constexpr int64_t kCacheVecMax = 12800;  // 200 KB of fp16 (8 elements per vector)
 constexpr int kWarps = kRowThreads / 32;
+constexpr int kRowsPrefetchChunks = 2;  // L2 prefetch distance of pass 2, in chunks
 
 // ---- (max, sum of 2^(x - max)) pairs -----------------------------------------
 struct MD {
@@ -105,6 +106,12 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
   }
   __syncthreads();
   return sh[NW];
+}
+
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, a multiple of 16
+// bytes); nothing waits for it.
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Two floats to fp16x2 (lo in the low half), saturated to the finite range.
@@ -224,6 +231,19 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       // 32-bit vector indices (nvec < 2^27): less index arithmetic per vector
       const int step = (int)blockDim.x;
       const int nv = (int)nvec;
+      // Pass 2 streams both rows from DRAM. One thread keeps bulk L2
+      // prefetches a few chunks (2 * step vectors of each row) ahead of the
+      // block, so that the loads find their lines in L2 instead of waiting for
+      // DRAM with only four 16-byte loads in flight per thread.
+      const int chunk = 2 * step;
+      auto prefetch_chunk = [&](int c0) {
+        if (a.rows_prefetch && threadIdx.x == 0 && c0 < nv) {
+          const uint32_t bytes = (uint32_t)((nv - c0 < chunk ? nv - c0 : chunk) * N * sizeof(T));
+          l2_prefetch(zs + (int64_t)c0 * N, bytes);
+          l2_prefetch(zt + (int64_t)c0 * N, bytes);
+        }
+      };
+      for (int c = 0; c < kRowsPrefetchChunks; ++c) prefetch_chunk(c * chunk);
       const int ncache = (int)(nvec < a.cache_vec ? nvec : a.cache_vec);
       uint4* cache = reinterpret_cast<uint4*>(xm_cache);
       auto pass2_vec = [&](const float (&xs)[N], const float (&xt)[N], int v) {
@@ -245,6 +265,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       int i = (int)threadIdx.x;
       // two vectors per iteration: four 16-byte loads in flight per thread
       for (; i + step < nv; i += 2 * step) {
+        prefetch_chunk(i + kRowsPrefetchChunks * chunk);  // thread 0: i is the chunk start
         float xs[N], xt[N], xs2[N], xt2[N];
         V::load(zs + i * N, xs);
         V::load(zt + i * N, xt);
@@ -454,6 +475,10 @@ cudaError_t launch_rows_t(JsdRowArgs a, cudaStream_t st) {
       if (env[0] == '0') a.cache_vec = 0;
     smem = (size_t)a.cache_vec * 16;
   }
+  // FLJSD_ROWS_PREFETCH=0 turns pass 2's L2 prefetch off
+  a.rows_prefetch = 1;
+  if (const char* env = getenv("FLJSD_ROWS_PREFETCH"))
+    if (env[0] == '0') a.rows_prefetch = 0;
   k_jsd_rows<T, BRANCH><<<(unsigned)grid, kRowThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
