@@ -225,12 +225,14 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
                              int64_t ldb, int32_t b_mn, void* d, int64_t ldd, int64_t m,
                              int64_t n, int64_t k, int32_t accumulate, int32_t* status,
                              int32_t flags, fljsd_stream_t stream);
-/* flags of fljsd_gemm_bf16: by default pairs of 128-row blocks of D run as
- * CTA pairs (2-CTA clusters, tcgen05.mma.cta_group::2) that compute a
- * 256 x 256 tile together, each CTA copying only its own rows of A and half
- * of the B tile; FLJSD_GEMM_SINGLE_CTA runs one CTA per 128 x 256 tile. The
- * results are identical. The environment variable FLJSD_GEMM_PAIR=0 selects
- * one CTA per tile for every GEMM of the library (read at each launch). */
+/* flags of fljsd_gemm_bf16: by default, for contractions at least 1024 deep,
+ * pairs of 128-row blocks of D run as CTA pairs (2-CTA clusters,
+ * tcgen05.mma.cta_group::2) that compute a 256 x 256 tile together, each CTA
+ * copying only its own rows of A and half of the B tile;
+ * FLJSD_GEMM_SINGLE_CTA runs one CTA per 128 x 256 tile. The results are
+ * identical. The environment variable FLJSD_GEMM_PAIR (read at each launch)
+ * selects for every GEMM of the library: 0 one CTA per tile, 2 CTA pairs at
+ * any contraction depth. */
 #define FLJSD_GEMM_SINGLE_CTA 1
 /* Test of the failure path: the kernel's copy warp issues nothing, so its
  * first bounded wait expires after 50 ms; *status then holds

@@ -120,9 +120,14 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   if (!tc_gemm_supported(g)) return cudaErrorInvalidValue;
   const int64_t mblocks = (g.m + BM - 1) / BM;
   // split-K (below) for outputs with too few tiles for the GPU; otherwise
-  // pairs of m-blocks run as CTA pairs wherever there are two m-blocks to
-  // pair. FLJSD_GEMM_PAIR=0 in the environment selects one CTA per tile for
-  // every call (both schedules compute identical results).
+  // pairs of m-blocks run as CTA pairs wherever there are two m-blocks to pair
+  // and the contraction is at least 16 k-blocks deep (K >= 1024): below that
+  // the epilogue sets the pace and a pair's accumulator hand-offs cost more
+  // than its halved B copies save (measured on the chunked grad_weight's
+  // read-modify-write: K = 128 21.6 vs 20.5 ms, K = 512 8.53 vs 8.35 ms per
+  // headline step). FLJSD_GEMM_PAIR=0 in the environment selects one CTA per
+  // tile for every call, FLJSD_GEMM_PAIR=2 CTA pairs at any depth (both
+  // schedules compute identical results).
   const char* senv = getenv("FLJSD_GEMM_SPLITK");
   const bool split_off = senv != nullptr && senv[0] == '0';
   int splits = 1;
@@ -135,7 +140,9 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   }
   const char* penv_pair = getenv("FLJSD_GEMM_PAIR");
   const bool pair_off = penv_pair != nullptr && penv_pair[0] == '0';
-  const bool pair = mblocks >= 2 && splits <= 1 && !g.single_cta && !pair_off;
+  const bool pair_any = penv_pair != nullptr && penv_pair[0] == '2';
+  const bool deep = (g.k + BK - 1) / BK >= 16;
+  const bool pair = mblocks >= 2 && splits <= 1 && !g.single_cta && !pair_off && (deep || pair_any);
   CUtensorMap ma, mb;
   bool ok;
   if (g.a_mn)  // A stored [k x m]

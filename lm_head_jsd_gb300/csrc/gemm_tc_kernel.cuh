@@ -121,8 +121,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-// CL: acquire at cluster scope (the phase completes through release arrivals
-// of threads in the other CTA of a pair).
+// CL: acquire at cluster scope (the phase completes through arrivals of
+// threads in the other CTA of a pair).
 template <bool CL = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -150,15 +150,9 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Arrive (release, cluster scope) on an mbarrier of another CTA of the
-// cluster, given its shared::cluster address (map_to_cta).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-// The same without release semantics, for hand-overs that order only
-// asynchronous work (the MMAs' reads of a stage before the next copies into
-// it).
+// Arrive (relaxed, cluster scope) on an mbarrier of another CTA of the
+// cluster, given its shared::cluster address (map_to_cta): for hand-overs that
+// order only asynchronous work (see the kernel's barrier notes).
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
@@ -566,12 +560,13 @@ static __device__ __noinline__ void store_chunk_generic(const KParams& p, float*
 //                  arrive, once per fill, after expecting both CTAs' bytes)
 //   tmem_full[a]   accumulator a complete | same | relayed by the leader's epilogue
 //   tmem_empty[a]  4G epilogue warps drained accumulator a | 4G warps of each CTA | unused
-// Stage data moves only through the asynchronous proxy (TMA writes, MMA
-// reads), ordered by the barriers' transaction counts and tcgen05.commit, so
-// the stage waits are CTA-scoped and the leader hands a stage on with a
-// relaxed remote arrive (a release at cluster scope cost ~0.5 us per fill and
-// halved the pair's throughput, measured). The accumulator hand-offs, once
-// per tile, release and acquire at cluster scope.
+// Every hand-over between the two CTAs orders only asynchronous work (TMA
+// writes and MMA reads of a stage; MMA writes and tcgen05.ld reads of the
+// accumulator, the latter completed by tcgen05.wait::ld before the arrive),
+// so the remote arrives are relaxed: a release at cluster scope waits for the
+// arriving thread's earlier global stores and cost ~0.5 us per arrive
+// (measured: it halved the pair's throughput as the stage hand-over and
+// slowed epilogue-bound contractions by 60% as the accumulator hand-offs).
 template <bool A_MN, bool B_MN, bool PAIR, int G, int EPI>
 __global__ void __launch_bounds__(threads_for(G), 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -855,7 +850,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
         // the leader's first epilogue warp tells the other CTA that its rows
         // of the accumulator are complete too (the MMAs were issued here)
         if (PAIR && ok && leader && ew == 0)
-          mbar_arrive_remote(map_to_cta(smem_u32(&cb->tmem_full[acc]), 1));
+          mbar_arrive_remote_relaxed(map_to_cta(smem_u32(&cb->tmem_full[acc]), 1));
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
@@ -1046,7 +1041,7 @@ __global__ void __launch_bounds__(threads_for(G), 1)
         // the accumulator's MMAs are the leader's: its barrier counts the
         // epilogue warps of both CTAs
         if (PAIR && !leader)
-          mbar_arrive_remote(map_to_cta(smem_u32(&cb->tmem_empty[acc]), 0));
+          mbar_arrive_remote_relaxed(map_to_cta(smem_u32(&cb->tmem_empty[acc]), 0));
         else
           mbar_arrive(smem_u32(&cb->tmem_empty[acc]));
       }

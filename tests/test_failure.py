@@ -11,13 +11,15 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("acc", [0, 1], ids=["store", "accumulate"])
 @pytest.mark.parametrize("pairs", [True, False], ids=["pairs", "single"])
-def test_gemm_wait_timeout_is_reported_and_the_context_survives(pairs, acc):
+def test_gemm_wait_timeout_is_reported_and_the_context_survives(pairs, acc, monkeypatch):
     """With acc = 1 the stored output is read ahead by the prefetch warp, whose
     ring of slabs fills and whose waits then expire as well. In a CTA pair
     both CTAs' waits expire (each on its own clock) and both leave through
     the cluster barrier at the exit."""
     from lm_head_jsd_gb300 import _lib
 
+    if pairs:  # CTA pairs at this contraction depth too
+        monkeypatch.setenv("FLJSD_GEMM_PAIR", "2")
     m, n, k = 512, 512, 256
     g = torch.Generator(device="cuda").manual_seed(3)
     a = torch.randn(m, k, generator=g, device="cuda").to(torch.bfloat16)

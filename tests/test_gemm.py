@@ -32,8 +32,11 @@ def _ref(a, a_mn, b, b_mn):
 @pytest.mark.parametrize("flags", [0, 1], ids=["pairs", "single"])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_gemm_layouts(a_mn, b_mn, shape, flags):
+def test_gemm_layouts(a_mn, b_mn, shape, flags, monkeypatch):
     from lm_head_jsd_gb300 import fljsd_gemm_bf16
+
+    if flags == 0:  # CTA pairs at every contraction depth
+        monkeypatch.setenv("FLJSD_GEMM_PAIR", "2")
 
     m, n, k = shape
     g = torch.Generator(device="cuda").manual_seed(m * 7 + n * 3 + k)
@@ -90,12 +93,14 @@ def test_gemm_rejects_bad_arguments():
 @pytest.mark.parametrize("shape", [(1000, 777, 300), (256, 512, 64), (384, 1000, 1000),
                                    (4096, 4096, 512)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_gemm_pairs_and_single_ctas_agree_bitwise(a_mn, b_mn, shape):
+def test_gemm_pairs_and_single_ctas_agree_bitwise(a_mn, b_mn, shape, monkeypatch):
     """A CTA pair computes a 256-row tile with one MMA instruction over both
     CTAs' shared memory; one CTA computes 128 rows. The products and their
     fp32 accumulation order are the same, so both schedules give identical
     bits (including an odd m-block count, whose last pair has an empty half)."""
     from lm_head_jsd_gb300 import fljsd_gemm_bf16
+
+    monkeypatch.setenv("FLJSD_GEMM_PAIR", "2")  # pairs at every contraction depth
 
     m, n, k = shape
     g = torch.Generator(device="cuda").manual_seed(11 + m + n + k)
@@ -120,6 +125,8 @@ def test_gemm_pairs_and_single_ctas_agree_bitwise(a_mn, b_mn, shape):
                                    (5000, 4096, 64)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_gemm_accumulate_prefetch_matches_plain_loads(a_mn, b_mn, shape, flags, monkeypatch):
+    if flags == 0:  # CTA pairs at every contraction depth
+        monkeypatch.setenv("FLJSD_GEMM_PAIR", "2")
     """The accumulating epilogue reads the old values from slabs copied ahead by
     TMA (shallow, middle and deep operand rings by contraction length); with the
     copy turned off it reads them with plain loads. Same arithmetic, so the
@@ -154,6 +161,8 @@ def test_gemm_accumulate_prefetch_matches_plain_loads(a_mn, b_mn, shape, flags, 
 @pytest.mark.parametrize("shape", [(1000, 1000, 128), (129, 4096, 640), (300, 264, 4096)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_gemm_staged_output_matches_plain_stores(a_mn, b_mn, shape, flags, monkeypatch):
+    if flags == 0:  # CTA pairs at every contraction depth
+        monkeypatch.setenv("FLJSD_GEMM_PAIR", "2")
     """A plain (non-accumulating) bf16 output goes through shared-memory staging
     buffers and TMA stores; with staging turned off each thread stores its row.
     Same rounding, so the results agree bitwise; the stores are clipped at the
