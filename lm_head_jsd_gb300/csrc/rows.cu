@@ -61,7 +61,7 @@ __device__ __forceinline__ void md_fold(MD& s, const float (&z)[N], float c) {
 
 // Block-wide reductions in a fixed order (deterministic): a butterfly inside
 // each warp, the per-warp results through shared memory, a butterfly over
-// them in warp 0, and the total broadcast from slot NW. sh holds NW + 1.
+// them in warp 0, and the total broadcast from the slot after theirs.
 __device__ __forceinline__ MD warp_md(MD v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -70,19 +70,31 @@ __device__ __forceinline__ MD warp_md(MD v) {
   }
   return v;
 }
+// The student's and the teacher's (m, d) together: one pair of barriers.
+// sh holds 2 * (NW + 1).
 template <int NW>
-__device__ __forceinline__ MD block_md(MD v, MD* sh) {
+__device__ __forceinline__ void block_md2(MD& va, MD& vb, MD* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_md(v);
-  if (lane == 0) sh[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    MD u = lane < NW ? sh[lane] : MD{-CUDART_INF_F, 0.f};
-    u = warp_md(u);
-    if (lane == 0) sh[NW] = u;
+  va = warp_md(va);
+  vb = warp_md(vb);
+  if (lane == 0) {
+    sh[2 * warp] = va;
+    sh[2 * warp + 1] = vb;
   }
   __syncthreads();
-  return sh[NW];
+  if (warp == 0) {
+    MD ua = lane < NW ? sh[2 * lane] : MD{-CUDART_INF_F, 0.f};
+    MD ub = lane < NW ? sh[2 * lane + 1] : MD{-CUDART_INF_F, 0.f};
+    ua = warp_md(ua);
+    ub = warp_md(ub);
+    if (lane == 0) {
+      sh[2 * NW] = ua;
+      sh[2 * NW + 1] = ub;
+    }
+  }
+  __syncthreads();
+  va = sh[2 * NW];
+  vb = sh[2 * NW + 1];
 }
 
 __device__ __forceinline__ float2 warp_sum2(float2 v) {
@@ -112,6 +124,14 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
 // bytes); nothing waits for it.
 __device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// The 16-byte units that lie wholly inside [p, p + bytes) into L2 (a
+// prefetch; bytes outside the span are not touched).
+__device__ __forceinline__ void l2_prefetch_span(const void* p, size_t bytes) {
+  const uintptr_t b = ((uintptr_t)p + 15u) & ~(uintptr_t)15u;
+  const uintptr_t e = ((uintptr_t)p + bytes) & ~(uintptr_t)15u;
+  if (e > b) l2_prefetch(reinterpret_cast<const void*>(b), (uint32_t)(e - b));
 }
 
 // Two floats to fp16x2 (lo in the low half), saturated to the finite range.
@@ -144,7 +164,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
   using V = Vec<T>;
   constexpr bool PREC = sizeof(T) == 4;
   constexpr int N = V::N;
-  __shared__ MD sh_md[kWarps + 1];
+  __shared__ MD sh_md[2 * (kWarps + 1)];
   __shared__ float2 sh_s[kWarps + 1];
   extern __shared__ uint4 xm_cache[];  // lean path: fp16 X - log M of cache_vec vectors
 
@@ -158,7 +178,28 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
     const int64_t grow = a.row0 + r;
     T* zs = reinterpret_cast<T*>(a.zs) + r * a.ld;
     const T* zt = reinterpret_cast<const T*>(a.zt) + r * a.ld;
+    if (threadIdx.x == 0 && a.rows_prefetch && r + gridDim.x < a.rows) {
+      // the next row's label and pass-1 partials into L2, a row ahead: they
+      // are the first loads of the row and nothing else would hide their latency
+      const int64_t rn = r + gridDim.x;
+      if (a.labels != nullptr)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.labels + a.row0 + rn) : "memory");
+      if (a.stats_s != nullptr) {
+        l2_prefetch_span(a.stats_s + rn * a.ntiles, (size_t)a.ntiles * sizeof(float2));
+        l2_prefetch_span(a.stats_t + rn * a.ntiles, (size_t)a.ntiles * sizeof(float2));
+      }
+    }
     const bool valid = (a.labels == nullptr) || (a.labels[grow] != a.ignore_index);
+    if (BRANCH == 2 && !PREC && valid && a.rows_prefetch && threadIdx.x == 0) {
+      // the head of both rows, while pass 1's partials are combined (pass 2
+      // keeps its prefetches ahead of the block from there on)
+      const size_t head = (size_t)(nvec < 2 * kRowsPrefetchChunks * (int64_t)blockDim.x
+                                       ? nvec
+                                       : 2 * kRowsPrefetchChunks * (int64_t)blockDim.x) *
+                          N * sizeof(T);
+      l2_prefetch_span(zs, head);
+      l2_prefetch_span(zt, head);
+    }
 
     float w = 0.f;  // row weight w_r
     if (valid) {
@@ -206,8 +247,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
         md_fold<1>(mb, xt, c);
       }
     }
-    const MD ra = block_md<kWarps>(ma, sh_md);
-    const MD rb = block_md<kWarps>(mb, sh_md);
+    block_md2<kWarps>(ma, mb, sh_md);
+    const MD ra = ma, rb = mb;
     // log2 Q_j = z_j * c - m_a - log2 d_a, formed as fma(z, c, -m) - log2 d so
     // that the exact product is rounded once relative to the row maximum.
     // A one-element row has log-prob 0 whatever its logit.
@@ -243,7 +284,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
           l2_prefetch(zt + (int64_t)c0 * N, bytes);
         }
       };
-      for (int c = 0; c < kRowsPrefetchChunks; ++c) prefetch_chunk(c * chunk);
+      // (the first kRowsPrefetchChunks chunks were prefetched at the row's start)
       const int ncache = (int)(nvec < a.cache_vec ? nvec : a.cache_vec);
       uint4* cache = reinterpret_cast<uint4*>(xm_cache);
       auto pass2_vec = [&](const float (&xs)[N], const float (&xt)[N], int v) {
@@ -332,7 +373,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
         lean_terms(V::one(zs + j), V::one(zt + j), cz, oa, ob, beta, omb, Q, P, xm, ym);
         V::put(zs + j, Q * fmaf(k1, xm, -k2));
       }
-      __syncthreads();  // the cache is rewritten by the next row's pass 2
+      // no barrier here: the next row's pass-1 reduction (block_md2) holds
+      // every thread before anyone writes the cache in its pass 2
       continue;
     }
 
