@@ -363,6 +363,40 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       // walk the row backwards: the lines pass 2 read last are the likeliest
       // to still be in L2
       int i3 = nv - 1 - (int)threadIdx.x;
+      // four vectors per iteration; where all four are cached (the row's
+      // first ncache vectors), their loads are all issued before any of them
+      // is computed: more L2 reads in flight per thread (measured: 0.361 ->
+      // 0.340 ms on 2048 full-length rows)
+      for (; i3 - 3 * step >= 0; i3 -= 4 * step) {
+        if (i3 >= ncache) {  // not all four cached: one at a time
+          pass3_vec(i3);
+          pass3_vec(i3 - step);
+          pass3_vec(i3 - 2 * step);
+          pass3_vec(i3 - 3 * step);
+          continue;
+        }
+        // four cached vectors: all loads first
+        float xs[4][N];
+        uint4 hv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          V::load(zs + (i3 - u * step) * N, xs[u]);
+          hv[u] = cache[i3 - u * step];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t h[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 xm2 = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
+            const float X0 = __fmaf_rn(xs[u][2 * e], cz, -oa);
+            const float X1 = __fmaf_rn(xs[u][2 * e + 1], cz, -oa);
+            xs[u][2 * e] = ex2(X0) * fmaf(k1, xm2.x, -k2);
+            xs[u][2 * e + 1] = ex2(X1) * fmaf(k1, xm2.y, -k2);
+          }
+          V::store(zs + (i3 - u * step) * N, xs[u]);
+        }
+      }
       for (; i3 - step >= 0; i3 -= 2 * step) {
         pass3_vec(i3);
         pass3_vec(i3 - step);
