@@ -159,6 +159,23 @@ __device__ __forceinline__ void lean_terms(float zs, float zt, float c, float oa
   ym = Y2 - lM;
 }
 
+// lean_terms for two elements at a time, on the packed fp32x2 FMA / ADD / MUL
+// instructions (each lane rounds exactly like the scalar operation, so the
+// terms are bitwise those of lean_terms). c2 = (c, c), noa = (-oa, -oa), ...
+__device__ __forceinline__ void lean_terms2(float2 zs, float2 zt, float2 c2, float2 noa,
+                                            float2 nob, float2 beta2, float2 omb2, float2& Q,
+                                            float2& P, float2& xm, float2& ym) {
+  const float2 X2 = __ffma2_rn(zs, c2, noa);
+  const float2 Y2 = __ffma2_rn(zt, c2, nob);
+  Q = make_float2(ex2(X2.x), ex2(X2.y));
+  P = make_float2(ex2(Y2.x), ex2(Y2.y));
+  const float2 M = __ffma2_rn(omb2, Q, __ffma2_rn(beta2, P, make_float2(1.17549435e-38f, 1.17549435e-38f)));
+  const float2 lM = make_float2((X2.x == Y2.x) ? X2.x : lg2(M.x), (X2.y == Y2.y) ? X2.y : lg2(M.y));
+  const float2 m1 = make_float2(-1.f, -1.f);
+  xm = __ffma2_rn(lM, m1, X2);  // X2 - lM, exact product, one rounding
+  ym = __ffma2_rn(lM, m1, Y2);
+}
+
 template <typename T, int BRANCH>
 __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
   using V = Vec<T>;
@@ -269,6 +286,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
     if (BRANCH == 2 && !PREC && fabsf(ma_) < 64.f && fabsf(mb_) < 64.f) {
       const float oa = ma_ + lda, ob = mb_ + ldb;
       float accq = 0.f, accp = 0.f;
+      // pair forms of the constants, and pair accumulators (even and odd
+      // elements, added at the end of the row)
+      const float2 c2 = make_float2(cz, cz), noa = make_float2(-oa, -oa), nob = make_float2(-ob, -ob);
+      const float2 beta2 = make_float2(beta, beta), omb2 = make_float2(omb, omb);
+      float2 accq2 = make_float2(0.f, 0.f), accp2 = make_float2(0.f, 0.f);
       // 32-bit vector indices (nvec < 2^27): less index arithmetic per vector
       const int step = (int)blockDim.x;
       const int nv = (int)nvec;
@@ -290,12 +312,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       auto pass2_vec = [&](const float (&xs)[N], const float (&xt)[N], int v) {
         float xm8[N];
 #pragma unroll
-        for (int k = 0; k < N; ++k) {
-          float Q, P, xm, ym;
-          lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
-          accq = fmaf(Q, xm, accq);
-          accp = fmaf(P, ym, accp);
-          xm8[k] = xm;
+        for (int k = 0; k < N; k += 2) {
+          float2 Q, P, xm, ym;
+          lean_terms2(make_float2(xs[k], xs[k + 1]), make_float2(xt[k], xt[k + 1]), c2, noa, nob,
+                      beta2, omb2, Q, P, xm, ym);
+          accq2 = __ffma2_rn(Q, xm, accq2);
+          accp2 = __ffma2_rn(P, ym, accp2);
+          xm8[k] = xm.x;
+          xm8[k + 1] = xm.y;
         }
         if (v < ncache) {
           // saturated to the fp16 range: where |xm| is that large Q is 0
@@ -327,6 +351,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
         accq = fmaf(Q, xm, accq);
         accp = fmaf(P, ym, accp);
       }
+      accq += accq2.x + accq2.y;
+      accp += accp2.x + accp2.y;
       const float2 tot = block_sum2<kWarps>(make_float2(accq, accp), sh_s);  // also orders the cache
       const float S2 = omb * tot.x;
       const float L2 = fmaf(beta, tot.y, S2);
@@ -334,6 +360,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       // dz = ln2 * scale * Q * ((1-beta) xm - S)
       const float k0 = 0.6931471805599453f * w * a.inv_temperature * a.loss_scale;
       const float k1 = k0 * omb, k2 = k0 * S2;
+      const float2 k12 = make_float2(k1, k1), nk22 = make_float2(-k2, -k2);
       auto pass3_vec = [&](int v) {
         float xs[N];
         V::load(zs + v * N, xs);
@@ -343,19 +370,23 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 xm2 = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
-            const float X0 = __fmaf_rn(xs[2 * e], cz, -oa);
-            const float X1 = __fmaf_rn(xs[2 * e + 1], cz, -oa);
-            xs[2 * e] = ex2(X0) * fmaf(k1, xm2.x, -k2);
-            xs[2 * e + 1] = ex2(X1) * fmaf(k1, xm2.y, -k2);
+            const float2 X = __ffma2_rn(make_float2(xs[2 * e], xs[2 * e + 1]), c2, noa);
+            const float2 t = __ffma2_rn(k12, xm2, nk22);
+            const float2 dz = __fmul2_rn(make_float2(ex2(X.x), ex2(X.y)), t);
+            xs[2 * e] = dz.x;
+            xs[2 * e + 1] = dz.y;
           }
         } else {
           float xt[N];
           V::load(zt + v * N, xt);
 #pragma unroll
-          for (int k = 0; k < N; ++k) {
-            float Q, P, xm, ym;
-            lean_terms(xs[k], xt[k], cz, oa, ob, beta, omb, Q, P, xm, ym);
-            xs[k] = Q * fmaf(k1, xm, -k2);
+          for (int k = 0; k < N; k += 2) {
+            float2 Q, P, xm, ym;
+            lean_terms2(make_float2(xs[k], xs[k + 1]), make_float2(xt[k], xt[k + 1]), c2, noa, nob,
+                        beta2, omb2, Q, P, xm, ym);
+            const float2 dz = __fmul2_rn(Q, __ffma2_rn(k12, xm, nk22));
+            xs[k] = dz.x;
+            xs[k + 1] = dz.y;
           }
         }
         V::store(zs + v * N, xs);
@@ -389,10 +420,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 xm2 = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
-            const float X0 = __fmaf_rn(xs[u][2 * e], cz, -oa);
-            const float X1 = __fmaf_rn(xs[u][2 * e + 1], cz, -oa);
-            xs[u][2 * e] = ex2(X0) * fmaf(k1, xm2.x, -k2);
-            xs[u][2 * e + 1] = ex2(X1) * fmaf(k1, xm2.y, -k2);
+            const float2 X = __ffma2_rn(make_float2(xs[u][2 * e], xs[u][2 * e + 1]), c2, noa);
+            const float2 t = __ffma2_rn(k12, xm2, nk22);
+            const float2 dz = __fmul2_rn(make_float2(ex2(X.x), ex2(X.y)), t);
+            xs[u][2 * e] = dz.x;
+            xs[u][2 * e + 1] = dz.y;
           }
           V::store(zs + (i3 - u * step) * N, xs[u]);
         }
