@@ -27,6 +27,8 @@ using namespace rowmath;
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+// vectors each thread loads before it stores in the lean pass 2 (bytes in flight)
+constexpr int kCeUnroll = 2;
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -54,28 +56,57 @@ __device__ __forceinline__ MD md_combine(MD a, MD b) {
                    (b.m == -INFINITY ? 0.f : b.d * ex2(b.m - m))};
 }
 
-__device__ __forceinline__ void block_md2(MD& v, float& s, MD* shm, float* shs) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Block-wide (m, d) and sum in a fixed order (deterministic): butterflies in
+// each warp, then one butterfly over the per-warp results in warp 0, whose
+// total every thread reads from the slot after theirs (shm, shs hold
+// kWarps + 1).
+__device__ __forceinline__ void warp_md_sum(MD& v, float& s) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     MD u{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.d, o)};
     v = md_combine(v, u);
     s += __shfl_xor_sync(0xffffffffu, s, o);
   }
+}
+__device__ __forceinline__ void block_md2(MD& v, float& s, MD* shm, float* shs) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  warp_md_sum(v, s);
   if (lane == 0) {
     shm[warp] = v;
     shs[warp] = s;
   }
   __syncthreads();
-  MD r = shm[0];
-  float t = shs[0];
-  for (int w = 1; w < kWarps; ++w) {
-    r = md_combine(r, shm[w]);
-    t += shs[w];
+  if (warp == 0) {
+    MD u = lane < kWarps ? shm[lane] : MD{-INFINITY, 0.f};
+    float t = lane < kWarps ? shs[lane] : 0.f;
+    warp_md_sum(u, t);
+    if (lane == 0) {
+      shm[kWarps] = u;
+      shs[kWarps] = t;
+    }
   }
   __syncthreads();
-  v = r;
-  s = t;
+  v = shm[kWarps];
+  s = shs[kWarps];
+}
+
+// Eight bf16 (one 16-byte load) to fp32: exact, a shift into the high half.
+__device__ __forceinline__ void unpack_bf16x8(uint4 v, float (&o)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = __uint_as_float(w[i] << 16);
+    o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// Bulk prefetch of the 16-byte units wholly inside [p, p + bytes) into L2.
+__device__ __forceinline__ void l2_prefetch_span(const void* p, size_t bytes) {
+  const uintptr_t b = ((uintptr_t)p + 15u) & ~(uintptr_t)15u;
+  const uintptr_t e = ((uintptr_t)p + bytes) & ~(uintptr_t)15u;
+  if (e > b)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b), "r"((uint32_t)(e - b))
+                 : "memory");
 }
 
 // capped logit
@@ -88,8 +119,8 @@ template <typename T, bool CAP>
 __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
   using V = Vec<T>;
   constexpr int N = V::N;
-  __shared__ MD shm[kWarps];
-  __shared__ float shs[kWarps];
+  __shared__ MD shm[kWarps + 1];
+  __shared__ float shs[kWarps + 1];
   const float L2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
   const int n_valid = *a.n_valid;
   float w = 1.f;
@@ -163,6 +194,76 @@ __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
 
     // ---- pass 2: dlogits in place (and the sum of c when pass 1 was folded) ----
     float csum2 = 0.f;
+    if constexpr (!CAP && sizeof(T) == 2) {
+      // bf16 without a cap: kCeUnroll vectors per iteration with bulk L2
+      // prefetches two iterations ahead; the label's element is corrected once, by the
+      // thread whose vector holds it; the sum of c only where label smoothing
+      // needs it; packed fp32x2 arithmetic (each lane rounds as the scalar form)
+      const int step = (int)blockDim.x, nv = (int)nvec, chunk = kCeUnroll * step;
+      const bool need_sum = have_stats && a.eps != 0.f;
+      const int yv = (int)(y / N), yk = (int)(y % N);
+      const float2 l2e2 = make_float2(L2E, L2E), nm2 = make_float2(-m, -m);
+      const float2 nld2 = make_float2(-ld2, -ld2), gsm2 = make_float2(gsm, gsm);
+      const float2 neps2 = make_float2(-eps_v, -eps_v), w2 = make_float2(w, w);
+      if (threadIdx.x == 0)
+        l2_prefetch_span(zr, (size_t)(nv < 2 * chunk ? nv : 2 * chunk) * N * sizeof(T));
+      auto vec = [&](float (&zs)[N]) {
+#pragma unroll
+        for (int k = 0; k < N; k += 2) {
+          const float2 c = make_float2(zs[k], zs[k + 1]);
+          if (need_sum) csum2 += c.x + c.y;
+          const float2 x = __fadd2_rn(__ffma2_rn(c, l2e2, nm2), nld2);
+          const float2 dc = __ffma2_rn(make_float2(ex2(x.x), ex2(x.y)), gsm2, neps2);
+          const float2 g = __fmul2_rn(dc, w2);
+          zs[k] = g.x;
+          zs[k + 1] = g.y;
+        }
+      };
+      // element yk of a vector, read and written with compile-time indices (a
+      // runtime index would put the vector in local memory)
+      auto pick = [&](const float (&zs)[N]) {
+        float r = zs[0];
+#pragma unroll
+        for (int k = 1; k < N; ++k) r = k == yk ? zs[k] : r;
+        return r;
+      };
+      auto put = [&](float (&zs)[N], float val) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) zs[k] = k == yk ? val : zs[k];
+      };
+      // the label's element gets dc - (1 - eps), from its logit as loaded
+      auto label_dz = [&](float z) {
+        return (fmaf(ex2(__fmaf_rn(z, L2E, -m) - ld2), gsm, -eps_v) - onehot) * w;
+      };
+      int i = (int)threadIdx.x;
+      for (; i + (kCeUnroll - 1) * step < nv; i += kCeUnroll * step) {
+        if (threadIdx.x == 0 && i + 2 * chunk < nv)
+          l2_prefetch_span(zr + (int64_t)(i + 2 * chunk) * N,
+                           (size_t)(nv - (i + 2 * chunk) < chunk ? nv - (i + 2 * chunk) : chunk) *
+                               N * sizeof(T));
+        uint4 raw[kCeUnroll];  // packed bf16: 4 registers a vector in flight
+#pragma unroll
+        for (int u = 0; u < kCeUnroll; ++u)
+          raw[u] = *reinterpret_cast<const uint4*>(zr + (int64_t)(i + u * step) * N);
+#pragma unroll
+        for (int u = 0; u < kCeUnroll; ++u) {
+          float zs[N];
+          unpack_bf16x8(raw[u], zs);
+          const float yl = pick(zs);
+          vec(zs);
+          if (i + u * step == yv) put(zs, label_dz(yl));
+          V::store(zr + (int64_t)(i + u * step) * N, zs);
+        }
+      }
+      for (; i < nv; i += step) {
+        float z0[N];
+        V::load(zr + (int64_t)i * N, z0);
+        const float y0 = pick(z0);
+        vec(z0);
+        if (i == yv) put(z0, label_dz(y0));
+        V::store(zr + (int64_t)i * N, z0);
+      }
+    } else
     for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
       float zs[N];
       V::load(zr + i * N, zs);
@@ -194,7 +295,8 @@ __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
     }
     if (threadIdx.x == 0)
       a.loss_rows[grow] = lse - onehot * cy - eps_v * csum + a.lambda * lse * lse;
-    __syncthreads();
+    // no barrier here: the reduction slots a row reads (shm / shs[kWarps]) are
+    // written again only after the next row's first barrier
   }
 }
 
