@@ -301,6 +301,7 @@ def main():
         dist.barrier()
     clk = clocks.stop()
     launches = fl.fljsd_launch_count() - n_launch0
+    peak_bytes = torch.cuda.max_memory_allocated(dev)
     ms_total = ev0.elapsed_time(ev1)
     kinds = {}
     for k in ("gemm_logits", "jsd_rows", "gemm_grad_input", "gemm_grad_weight", "small"):
@@ -365,6 +366,10 @@ def main():
         "kernel_ms_per_step": {k: round(v[0] / max(steps_traced, 1), 4) for k, v in kinds.items()},
         "gpu_launches": launches,
         "clocks": clk,
+        "peak_device_memory": {
+            "bytes": int(peak_bytes), "gb": round(peak_bytes / 1e9, 3),
+            "what": "torch allocator peak through the timed region: inputs, outputs and the "
+                    "planned workspace (the library itself allocates nothing)"},
     }
     if args.e2e_steps > 0:
         out["e2e"] = run_e2e(torch, run, w, x_s, w_s, x_t, w_t, labels, args.e2e_steps, dist,
@@ -533,7 +538,16 @@ def run_flce_bench(args):
     g_ms = sum(kinds[k][0] for k in ("gemm_logits", "gemm_grad_input", "gemm_grad_weight"))
     g_n = sum(kinds[k][1] for k in ("gemm_logits", "gemm_grad_input", "gemm_grad_weight"))
     achieved = (flop / 3) / (g_ms / g_n / 1e3) / 1e12 if g_n else float("nan")
-    peak = peaks["bf16_tflops_sustained"]
+    # GEMM launches of a few ms inside the step: the burst peak is the
+    # denominator, the sustained one is given beside it
+    peak = peaks["bf16_tflops"]
+    peak_sus = peaks["bf16_tflops_sustained"]
+    # the row kernel reads the logits once and writes dlogits over them (the
+    # GEMM epilogue's per-128-column partials, 8 bytes each, come on top)
+    r_ms, r_n = kinds["jsd_rows"]
+    rows_bytes = (2 * bt * v * 2 + bt * ((v + 127) // 128) * 8) / run.plan.num_chunks
+    rows_gbs = rows_bytes / (r_ms / r_n / 1e3) / 1e9 if r_n else float("nan")
+    peak_bytes = torch.cuda.max_memory_allocated(dev)
     print(json.dumps({
         "metric": "fused-linear cross-entropy fwd+bwd tokens/s at H=4096,V=128256 bf16",
         "value": round(bt / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1,
@@ -544,10 +558,20 @@ def run_flce_bench(args):
                    "chunk_rows": int(run.plan.chunk_rows)},
         "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (3 launches per chunk)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None},
-        "roofline_step": {"flop": flop, "frac": round(flop / (peak * 1e12) * 1e3 / ms, 4)},
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_kind": f"bf16 burst ({peaks['source']})",
+                     "frac_of_sustained": round(achieved / peak_sus, 4)},
+        "roofline_step": {"flop": flop, "frac": round(flop / (peak * 1e12) * 1e3 / ms, 4),
+                          "peak": f"bf16 burst {peak} TFLOP/s ({peaks['source']})"},
+        "roofline_rows": {"bound": "hbm", "kernel": "k_ce_rows", "achieved": round(rows_gbs, 1),
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(rows_gbs / peaks["hbm_gbs"], 4),
+                          "algorithmic_bytes": "2*C*V*s (logits read, dlogits written) "
+                                               "+ 8 bytes per row per 128 columns"},
         "kernel_ms_per_step": {k: round(t / args.steps, 4) for k, (t, _) in kinds.items()},
-        "gpu_launches": fl.fljsd_launch_count() - n0}), flush=True)
+        "gpu_launches": fl.fljsd_launch_count() - n0,
+        "peak_device_memory": {"bytes": int(peak_bytes), "gb": round(peak_bytes / 1e9, 3)}}),
+        flush=True)
     return 0
 
 

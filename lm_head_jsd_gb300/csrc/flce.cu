@@ -43,7 +43,7 @@ struct CeRowArgs {
   const float2* stats;  // [rows x ntiles] partials of z * log2(e), or null
   int64_t ntiles;
   int reduction;
-  float eps, lambda, cap;
+  float eps, lambda, cap, inv_cap;
 };
 
 struct MD {
@@ -109,10 +109,14 @@ __device__ __forceinline__ void l2_prefetch_span(const void* p, size_t bytes) {
                  : "memory");
 }
 
-// capped logit
+// capped logit c = cap * tanh(z / cap), with t = tanh(z / cap) returned for
+// the derivative dc/dz = 1 - t^2 (inv_cap = 1 / cap, formed once on the host)
 template <bool CAP>
-__device__ __forceinline__ float capz(float z, float cap) {
-  return CAP ? cap * tanhf(z / cap) : z;
+__device__ __forceinline__ float capz(float z, float cap, float inv_cap, float* t = nullptr) {
+  if (!CAP) return z;
+  const float th = tanhf(z * inv_cap);
+  if (t) *t = th;
+  return cap * th;
 }
 
 template <typename T, bool CAP>
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
       if (threadIdx.x == 0) a.loss_rows[grow] = 0.f;
       continue;
     }
-    const float cy = capz<CAP>(V::one(zr + y), a.cap);
+    const float cy = capz<CAP>(V::one(zr + y), a.cap, a.inv_cap);
 
     // ---- pass 1: (max, sum 2^(x - max)) of x = c * log2(e), and sum of c ----
     MD md{-INFINITY, 0.f};
@@ -164,7 +168,7 @@ __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
         float vm = -INFINITY;
 #pragma unroll
         for (int k = 0; k < N; ++k) {
-          zs[k] = capz<CAP>(zs[k], a.cap);
+          zs[k] = capz<CAP>(zs[k], a.cap, a.inv_cap);
           csum += zs[k];
           vm = fmaxf(vm, __fmul_rn(zs[k], L2E));
         }
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
         for (int k = 0; k < N; ++k) md.d += ex2(__fmaf_rn(zs[k], L2E, -md.m));
       }
       for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-        const float c = capz<CAP>(V::one(zr + j), a.cap);
+        const float c = capz<CAP>(V::one(zr + j), a.cap, a.inv_cap);
         csum += c;
         const float x = __fmul_rn(c, L2E);
         if (x > md.m) {
@@ -269,23 +273,25 @@ __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
       V::load(zr + i * N, zs);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const float c = capz<CAP>(zs[k], a.cap);
+        float t = 0.f;
+        const float c = capz<CAP>(zs[k], a.cap, a.inv_cap, &t);
         csum2 += c;
         const float p = ex2(__fmaf_rn(c, L2E, -m) - ld2);
         float dc = fmaf(p, gsm, -eps_v);
         if (i * N + k == y) dc -= onehot;
-        if (CAP) dc *= 1.f - (c / a.cap) * (c / a.cap);
+        if (CAP) dc *= fmaf(-t, t, 1.f);
         zs[k] = dc * w;
       }
       V::store(zr + i * N, zs);
     }
     for (int64_t j = tail0 + threadIdx.x; j < a.v; j += blockDim.x) {
-      const float c = capz<CAP>(V::one(zr + j), a.cap);
+      float t = 0.f;
+      const float c = capz<CAP>(V::one(zr + j), a.cap, a.inv_cap, &t);
       csum2 += c;
       const float p = ex2(__fmaf_rn(c, L2E, -m) - ld2);
       float dc = fmaf(p, gsm, -eps_v);
       if (j == y) dc -= onehot;
-      if (CAP) dc *= 1.f - (c / a.cap) * (c / a.cap);
+      if (CAP) dc *= fmaf(-t, t, 1.f);
       V::put(zr + j, dc * w);
     }
     if (have_stats && a.eps != 0.f) {
@@ -480,6 +486,7 @@ fljsd_status fljsd_ce_forward(const fljsd_ce_problem* p, const fljsd_plan_t* pla
     ra.status = status; ra.loss_rows = loss_rows; ra.stats = st_done ? stats : nullptr;
     ra.ntiles = L.ntiles; ra.reduction = p->reduction; ra.eps = p->label_smoothing;
     ra.lambda = p->lse_square_scale; ra.cap = p->softcap;
+    ra.inv_cap = p->softcap > 0.f ? (float)(1.0 / (double)p->softcap) : 0.f;
     trace_begin(FLJSD_KERNEL_JSD_ROWS, stream);
     e = p->dtype == FLJSD_BF16 ? launch_ce_rows_t<__nv_bfloat16>(ra, stream)
                                : launch_ce_rows_t<float>(ra, stream);
