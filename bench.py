@@ -230,6 +230,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--ref-rows", type=int, default=16,
                     help="rows per step of the reference (oracle) arm")
+    ap.add_argument("--ce-bt", type=int, default=8192,
+                    help="rows of the cross-entropy path (--path flce)")
     ap.add_argument("--path", default="fljsd", choices=["fljsd", "jsd_logspace", "tvd", "flce"],
                     help="fljsd: the fused-linear JSD (the headline); the others measure the "
                          "distance kernels over given distributions")
@@ -503,7 +505,7 @@ def run_flce_bench(args):
     import lm_head_jsd_gb300 as fl
     from lm_head_jsd_gb300 import FusedLinearCrossEntropy
 
-    bt, h, v = 8192, 4096, 128256
+    bt, h, v = args.ce_bt, 4096, 128256
     dev = torch.device("cuda", 0)
     x, w, labels = jsd_inputs.make_ce_inputs(bt, h, v, "bf16", 200, device=str(dev))
     run = FusedLinearCrossEntropy(bt, h, v, torch.bfloat16, chunk_rows=args.chunk_rows,

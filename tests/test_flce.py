@@ -61,6 +61,44 @@ def test_flce_chunking(chunk, acc):
     compare(out, ref, "bf16", f"flce chunk={chunk} acc32={acc}")
 
 
+# V = 20003 in bf16: 2500 vectors of 8 (the row kernel takes two per thread
+# while v + 1024 < 2500, then one) and a ragged tail of 3 elements
+LABEL_POSITIONS = ([0, 1, 2, 3, 4, 5, 6, 7]  # every lane of the first vector
+                   + [8, 1023 * 8 + 7]  # the first vector's pair mate region
+                   + [1024 * 8 + k for k in (0, 3, 7)]  # second vector of a pair
+                   + [1475 * 8, 1476 * 8 + 5, 2048 * 8 + 3]  # last pair / one-at-a-time
+                   + [2499 * 8, 2499 * 8 + 7]  # last full vector
+                   + [20000, 20001, 20002])  # the tail
+
+
+@pytest.mark.parametrize("eps,lam", [(0.0, 0.0), (0.1, 1e-3)])
+def test_flce_label_positions(eps, lam):
+    """The bf16 row kernel corrects the label's element once, by the thread
+    whose vector holds it: labels on every lane of a vector, in both vectors
+    of the two-deep loop, in the one-at-a-time remainder, in the last full
+    vector and in the ragged tail; per-row losses and grad_input rows against
+    the oracle, row by row."""
+    v = 20003
+    lab = torch.tensor(LABEL_POSITIONS + [-100, 12345], dtype=torch.int64)
+    bt = lab.numel()
+    x, w, _ = jsd_inputs.make_ce_inputs(bt, 64, v, "bf16", 107)
+    kw = dict(label_smoothing=eps, lse_square_scale=lam)
+    (loss, gi, gw), _ = _gpu(x, w, lab, "bf16", reduction="none", **kw)
+    rows_ref, gi_ref, gw_ref = oracle.flce_ref(f64(x), f64(w), lab.numpy(), reduction="none",
+                                               **kw)
+    tol_loss, tol_grad = TOL["bf16"]
+    got_l, got_gi = f64(loss), f64(gi)
+    for r, y in enumerate(lab.tolist()):
+        if y == -100:
+            assert got_l[r] == 0.0 and np.all(got_gi[r] == 0.0), f"ignored row {r}"
+            continue
+        e = abs(got_l[r] - rows_ref[r]) / abs(rows_ref[r])
+        assert e <= tol_loss, f"label {y}: loss {got_l[r]} vs {rows_ref[r]} ({e:.3g})"
+        e = rel_fro(got_gi[r], gi_ref[r])
+        assert e <= tol_grad, f"label {y}: grad_input row error {e:.3g}"
+    assert rel_fro(f64(gw), gw_ref) <= tol_grad
+
+
 def test_flce_invalid_label_is_reported():
     from lm_head_jsd_gb300 import fljsd_workspace_status
 
