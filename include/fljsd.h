@@ -54,7 +54,7 @@ typedef struct CUstream_st* fljsd_stream_t;
 typedef enum {
   FLJSD_OK = 0,
   FLJSD_ERR_INVALID_ARG = 1, /* null pointer, bad size, beta or temperature, misalignment */
-  FLJSD_ERR_UNSUPPORTED = 2, /* valid but beyond the kernels' limits (sizes above 2^30) */
+  FLJSD_ERR_UNSUPPORTED = 2, /* valid but beyond the kernels' size limits (stated per call) */
   FLJSD_ERR_WORKSPACE = 3,   /* workspace smaller than the plan requires */
   FLJSD_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
   FLJSD_ERR_TIMEOUT = 5      /* a bounded device-side wait expired */
@@ -127,8 +127,9 @@ typedef struct {
  * memory per chunk is the two logits tensors, 2 * C * V * s bytes (PR 1352,
  * "Details", memory table), plus O(C) statistics and the (BT,) loss vector.
  * Host only; launches nothing. Returns FLJSD_ERR_INVALID_ARG for a bad
- * problem, FLJSD_ERR_UNSUPPORTED for shapes the kernels do not handle, and
- * FLJSD_ERR_WORKSPACE if not even one row fits.
+ * problem, FLJSD_ERR_UNSUPPORTED for shapes the kernels do not handle (bt or
+ * v above 2^30, h_s or h_t above 2^20), and FLJSD_ERR_WORKSPACE if not even
+ * one row fits.
  */
 fljsd_status fljsd_plan(const fljsd_problem* problem, size_t free_hbm_bytes,
                         fljsd_plan_t* out);
@@ -265,6 +266,15 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
  *
  * fljsd_scale -- x *= *grad_output in place (device fp32 scalar), skipped on
  * the device when it is 1: the backward of the two functions above.
+ *
+ * Errors (checked on the host before anything is launched):
+ * FLJSD_ERR_INVALID_ARG for rows or v <= 0, an unknown dtype or reduction, beta
+ * outside [0, 1], a null input, target, loss, gradient or workspace pointer, or
+ * one not 16-byte aligned (loss: 4 bytes; labels, when given: 16 bytes);
+ * FLJSD_ERR_UNSUPPORTED for rows or v above 2^31; FLJSD_ERR_WORKSPACE for a
+ * workspace below fljsd_rows_workspace_bytes(rows); FLJSD_ERR_CUDA when a
+ * launch fails. fljsd_scale: FLJSD_ERR_INVALID_ARG for an unknown dtype, n < 0,
+ * or a null or unaligned pointer.
  */
 size_t fljsd_rows_workspace_bytes(int64_t rows);
 fljsd_status fljsd_jsd_logspace(int64_t rows, int64_t v, int32_t dtype, float beta,
@@ -295,6 +305,20 @@ fljsd_status fljsd_scale(int32_t dtype, void* x, int64_t n, const float* grad_ou
  * workspace status word to FLJSD_ERR_INVALID_ARG (fljsd_workspace_status).
  * x [bt x h], w [v x h], grad_input [bt x h], grad_weight [v x h] in dtype.
  * Gradients are for an upstream gradient of 1 (fljsd_scale applies another).
+ *
+ * fljsd_ce_plan / fljsd_ce_forward follow fljsd_plan / fljsd_forward: every
+ * pointer is caller-owned device memory, 16-byte aligned (loss 4 bytes);
+ * grad_input and grad_weight are written in full and may be uninitialised; the
+ * workspace (plan->workspace_bytes, device, caller-owned) holds the logits of
+ * one chunk and the per-row statistics; the forward is asynchronous on
+ * `stream`. Errors, checked on the host before anything is launched:
+ * FLJSD_ERR_INVALID_ARG for a dimension <= 0, an unknown dtype, reduction or
+ * flag, label_smoothing outside [0, 1], a negative or non-finite
+ * lse_square_scale or softcap, or a null or unaligned pointer;
+ * FLJSD_ERR_UNSUPPORTED for bt or v above 2^30 or h above 2^20;
+ * FLJSD_ERR_WORKSPACE when the workspace is smaller than the plan's (or, in
+ * fljsd_ce_plan, when not even one row fits the budget); FLJSD_ERR_CUDA when a
+ * launch fails.
  */
 typedef struct {
   int64_t bt, h, v;

@@ -389,8 +389,8 @@ size_t fljsd_rows_workspace_bytes(int64_t rows) {
 static fljsd_status dist_common(int64_t rows, int64_t v, int32_t dtype, int32_t reduction,
                                 const void* x, const void* y, float* loss, void* grad,
                                 void* workspace, size_t workspace_bytes) {
-  if (rows <= 0 || v <= 0 || rows > (int64_t)1 << 31 || v > (int64_t)1 << 31)
-    return FLJSD_ERR_INVALID_ARG;
+  if (rows <= 0 || v <= 0) return FLJSD_ERR_INVALID_ARG;
+  if (rows > (int64_t)1 << 31 || v > (int64_t)1 << 31) return FLJSD_ERR_UNSUPPORTED;
   if (dtype != FLJSD_F32 && dtype != FLJSD_BF16) return FLJSD_ERR_INVALID_ARG;
   if (reduction < FLJSD_RED_NONE || reduction > FLJSD_RED_BATCHMEAN) return FLJSD_ERR_INVALID_ARG;
   if (!x || !y || !loss || !grad || !workspace) return FLJSD_ERR_INVALID_ARG;

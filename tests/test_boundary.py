@@ -134,6 +134,29 @@ def test_plan_rejects_bad_problems(L, field, value):
     assert e.value.status == 1
 
 
+@pytest.mark.parametrize("field,value", [("bt", (1 << 30) + 1), ("v", (1 << 30) + 1),
+                                         ("h_s", (1 << 20) + 1), ("h_t", (1 << 20) + 1)])
+def test_plan_reports_sizes_beyond_the_kernels(L, field, value):
+    """Valid problems beyond the kernels' index ranges (32-bit vector indices
+    along a row, grid limits) are refused with FLJSD_ERR_UNSUPPORTED, not
+    launched; the largest supported sizes plan."""
+    p = L.make_problem(16, 32, 32, 100, "bf16")
+    setattr(p, field, value)
+    with pytest.raises(L.FljsdError) as e:
+        L.fljsd_plan(p, 0)
+    assert e.value.status == 2
+    setattr(p, field, value - 1)
+    assert L.fljsd_plan(p, 0).chunk_rows > 0
+
+
+@pytest.mark.parametrize("bt,h,v", [((1 << 30) + 1, 32, 100), (16, (1 << 20) + 1, 100),
+                                    (16, 32, (1 << 30) + 1)])
+def test_ce_plan_reports_sizes_beyond_the_kernels(L, bt, h, v):
+    with pytest.raises(L.FljsdError) as e:
+        L.fljsd_ce_plan(L.make_ce_problem(bt, h, v, "bf16"), 0)
+    assert e.value.status == 2
+
+
 def _fake(addr=1 << 20):
     return addr  # an aligned, never dereferenced address
 
@@ -159,6 +182,33 @@ def test_forward_argument_checks_need_no_device(L):
     assert call(pl=other) == 1  # plan made for another problem
     bad = L.make_problem(16, 32, 32, 100, "bf16", beta=2.0)
     assert call(problem=bad) == 1
+
+
+@pytest.mark.parametrize("fn", ["jsd_logspace", "tvd"])
+def test_distance_argument_checks_need_no_device(L, fn):
+    """fljsd_jsd_logspace / fljsd_tvd refuse bad calls on the host, before any
+    launch: sizes (INVALID_ARG for <= 0, UNSUPPORTED above 2^31), dtype,
+    reduction, null or unaligned pointers, beta, and a short workspace."""
+    ws = L.fljsd_rows_workspace_bytes(16)
+
+    def call(rows=16, v=100, dtype="bf16", reduction="sum", x=_fake(), y=_fake(), loss=_fake(),
+             grad=_fake(), workspace=_fake(), ws_bytes=ws, beta=0.5, labels=None):
+        if fn == "jsd_logspace":
+            return L.fljsd_jsd_logspace(rows, v, dtype, beta, reduction, -100, x, y, labels, loss,
+                                        grad, workspace, workspace_bytes=ws_bytes, stream=0,
+                                        check=False)
+        return L.fljsd_tvd(rows, v, dtype, reduction, -100, x, y, labels, loss, grad, workspace,
+                           workspace_bytes=ws_bytes, stream=0, check=False)
+
+    assert call(rows=0) == 1 and call(v=0) == 1 and call(rows=-3) == 1
+    assert call(rows=(1 << 31) + 1) == 2 and call(v=(1 << 31) + 1) == 2
+    assert call(x=0) == 1 and call(y=0) == 1 and call(loss=0) == 1 and call(grad=0) == 1
+    assert call(workspace=0) == 1
+    assert call(x=_fake() + 8) == 1 and call(grad=_fake() + 4) == 1 and call(loss=_fake() + 2) == 1
+    assert call(labels=_fake() + 8) == 1
+    assert call(ws_bytes=ws - 1) == 3
+    if fn == "jsd_logspace":
+        assert call(beta=1.5) == 1 and call(beta=float("nan")) == 1
 
 
 def test_backward_argument_checks_need_no_device(L):
