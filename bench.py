@@ -387,49 +387,82 @@ def main():
 
 def run_e2e(torch, run, w, x_s, w_s, x_t, w_t, labels, steps, dist, world, dev):
     """The same step through the public API with the per-step inputs (hidden
-    states and labels) in pinned host memory: H2D copies, forward, backward and
-    the D2H read of the loss are all inside the timed region. The lm_head
-    weights stay resident (they are parameters, not per-step inputs)."""
+    states and labels) in pinned host memory, as a training loop runs it: the
+    inputs of step i + 1 are copied host -> device on a second stream into the
+    other of two device buffers while step i computes, and the loss of every
+    step is copied back and read on the host (one step behind the launches).
+    The timed region spans every copy and ends when the last loss is on the
+    host. The lm_head weights stay resident (they are parameters, not per-step
+    inputs)."""
     hx_s = x_s.cpu().pin_memory()
     hx_t = x_t.cpu().pin_memory()
     hlab = None if labels is None else labels.cpu().pin_memory()
-    host_loss = torch.empty(run.alloc_outputs()[0].shape, dtype=torch.float32).pin_memory()
-    dx_s = torch.empty_like(x_s)
-    dx_t = torch.empty_like(x_t)
-    dlab = None if labels is None else torch.empty_like(labels)
+    nloss = run.alloc_outputs()[0].numel()
+    host_loss = [torch.empty(nloss, dtype=torch.float32).pin_memory() for _ in range(2)]
+    dx_s = [torch.empty_like(x_s) for _ in range(2)]
+    dx_t = [torch.empty_like(x_t) for _ in range(2)]
+    dlab = [None if labels is None else torch.empty_like(labels) for _ in range(2)]
     loss, gi, gw = run.alloc_outputs()
     one = torch.ones(1, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    copy_stream = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]   # inputs of buffer b are on the device
+    consumed = [torch.cuda.Event() for _ in range(2)]  # the step reading buffer b is done
+    landed = [torch.cuda.Event() for _ in range(2)]   # the loss of the step is on the host
+    seen = []
 
-    def step():
-        dx_s.copy_(hx_s, non_blocking=True)
-        dx_t.copy_(hx_t, non_blocking=True)
-        if dlab is not None:
-            dlab.copy_(hlab, non_blocking=True)
-        run.forward(dx_s, w_s, dx_t, w_t, dlab, out=(loss, gi, gw), stream=stream)
+    def copy_in(b):
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(consumed[b])
+            dx_s[b].copy_(hx_s, non_blocking=True)
+            dx_t[b].copy_(hx_t, non_blocking=True)
+            if hlab is not None:
+                dlab[b].copy_(hlab, non_blocking=True)
+            copied[b].record(copy_stream)
+
+    def compute(b):
+        stream.wait_event(copied[b])
+        run.forward(dx_s[b], w_s, dx_t[b], w_t, dlab[b], out=(loss, gi, gw), stream=stream)
         run.backward(one, gi, gw, stream=stream)
-        host_loss.copy_(loss, non_blocking=True)
-        stream.synchronize()
-        return float(host_loss[0])
+        consumed[b].record(stream)
+        host_loss[b].copy_(loss.view(-1), non_blocking=True)
+        landed[b].record(stream)
 
-    for _ in range(2):
-        step()
+    def loop(n):
+        copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in((i + 1) % 2)
+            compute(i % 2)
+            if i >= 1:  # the previous step's loss, read on the host
+                landed[(i - 1) % 2].synchronize()
+                seen.append(float(host_loss[(i - 1) % 2][0]))
+        landed[(n - 1) % 2].synchronize()
+        seen.append(float(host_loss[(n - 1) % 2][0]))
+
+    for b in range(2):  # the first wait on a never-recorded event is a no-op
+        consumed[b].record(stream)
+    loop(2)
+    torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
-    torch.cuda.synchronize(dev)
+    seen.clear()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        step()
+    loop(steps)
     ms = reduce_max((time.perf_counter() - t0) * 1e3 / steps, dist, dev)
+    if len(seen) != steps or not all(v == v for v in seen):
+        raise RuntimeError("e2e: a step's loss did not come back")
     h2d = hx_s.numel() * hx_s.element_size() + hx_t.numel() * hx_t.element_size() + (
         0 if hlab is None else hlab.numel() * 8)
     return {"value": round(whole_job_tokens_per_s(world, w.bt, ms), 1), "unit": "tokens/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": host_loss.numel() * 4,
-            "what": "pinned-host X_s, X_t, labels -> device; fljsd_forward + fljsd_backward; "
-                    "loss -> host; grad_input and grad_weight stay on the device (training "
-                    "continues there); the lm_head weights are resident parameters; wall "
-                    "clock per step, stream synchronised every step"}
+            "d2h_bytes_per_step": nloss * 4,
+            "what": "pinned-host X_s, X_t, labels -> device every step on a copy stream, "
+                    "double-buffered so that step i+1's copy overlaps step i; fljsd_forward + "
+                    "fljsd_backward; every step's loss -> host and read there (one step behind); "
+                    "grad_input and grad_weight stay on the device (training continues there); "
+                    "the lm_head weights are resident parameters; wall clock from the first "
+                    "copy to the last loss on the host"}
 
 
 def run_dist_bench(args):
