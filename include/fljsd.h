@@ -226,7 +226,7 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
                              int64_t ldb, int32_t b_mn, void* d, int64_t ldd, int64_t m,
                              int64_t n, int64_t k, int32_t accumulate, int32_t* status,
                              int32_t flags, fljsd_stream_t stream);
-/* flags of fljsd_gemm_bf16: by default, for contractions at least 1024 deep,
+/* flags of fljsd_gemm_bf16: by default, for contractions at least 256 deep,
  * pairs of 128-row blocks of D run as CTA pairs (2-CTA clusters,
  * tcgen05.mma.cta_group::2) that compute a 256 x 256 tile together, each CTA
  * copying only its own rows of A and half of the B tile;

@@ -121,13 +121,14 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   const int64_t mblocks = (g.m + BM - 1) / BM;
   // split-K (below) for outputs with too few tiles for the GPU; otherwise
   // pairs of m-blocks run as CTA pairs wherever there are two m-blocks to pair
-  // and the contraction is at least 16 k-blocks deep (K >= 1024): below that
+  // and the contraction is at least 4 k-blocks deep (K >= 256): below that
   // the epilogue sets the pace and a pair's accumulator hand-offs cost more
   // than its halved B copies save (measured on the chunked grad_weight's
-  // read-modify-write: K = 128 21.6 vs 20.5 ms, K = 512 8.53 vs 8.35 ms per
-  // headline step). FLJSD_GEMM_PAIR=0 in the environment selects one CTA per
-  // tile for every call, FLJSD_GEMM_PAIR=2 CTA pairs at any depth (both
-  // schedules compute identical results).
+  // read-modify-write, grad_weight ms per headline step, pairs vs one CTA per
+  // tile: K = 128 21.31 vs 20.66, K = 256 12.06 vs 13.75, K = 512 8.22 vs
+  // 8.38). FLJSD_GEMM_PAIR=0 in the environment selects one CTA per tile for
+  // every call, FLJSD_GEMM_PAIR=2 CTA pairs at any depth (both schedules
+  // compute identical results).
   const char* senv = getenv("FLJSD_GEMM_SPLITK");
   const bool split_off = senv != nullptr && senv[0] == '0';
   int splits = 1;
@@ -141,7 +142,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   const char* penv_pair = getenv("FLJSD_GEMM_PAIR");
   const bool pair_off = penv_pair != nullptr && penv_pair[0] == '0';
   const bool pair_any = penv_pair != nullptr && penv_pair[0] == '2';
-  const bool deep = (g.k + BK - 1) / BK >= 16;
+  const bool deep = (g.k + BK - 1) / BK >= 4;
   const bool pair = mblocks >= 2 && splits <= 1 && !g.single_cta && !pair_off && (deep || pair_any);
   CUtensorMap ma, mb;
   bool ok;
