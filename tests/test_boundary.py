@@ -157,6 +157,48 @@ def test_ce_plan_reports_sizes_beyond_the_kernels(L, bt, h, v):
     assert e.value.status == 2
 
 
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "fljsd.h"
+
+int main(void) {
+  fljsd_problem p;
+  memset(&p, 0, sizeof p);
+  p.bt = 8192; p.h_s = 4096; p.h_t = 4096; p.v = 128256;
+  p.dtype = FLJSD_BF16; p.reduction = FLJSD_RED_BATCHMEAN;
+  p.beta = 0.5f; p.temperature = 1.0f; p.ignore_index = -100;
+  fljsd_plan_t plan;
+  fljsd_status st = fljsd_plan(&p, 0, &plan);
+  printf("%d %lld %lld %zu\n", (int)st, (long long)plan.chunk_rows,
+         (long long)plan.num_chunks, plan.workspace_bytes);
+  p.beta = 2.0f;
+  st = fljsd_plan(&p, 0, &plan);
+  printf("%d %s\n", (int)st, fljsd_status_string(st));
+  return 0;
+}
+"""
+
+
+def test_plain_c_client_links_and_plans(L, tmp_path):
+    """The boundary is plain C: a C99 program that includes only fljsd.h
+    compiles (-Wall -Werror), links against libfljsd.so and plans the headline
+    problem (one chunk, the workspace the Python binding reports) and gets a
+    synchronous INVALID_ARG for beta outside [0, 1]. No device call is made."""
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(L.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I",
+                    os.path.join(ROOT, "include"), str(src), "-o", str(exe), "-L", libdir,
+                    "-lfljsd", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    st, chunk, nchunks, ws = out[0].split()
+    ref = L.fljsd_plan(L.make_problem(8192, 4096, 4096, 128256, "bf16"), 0)
+    assert (int(st), int(chunk), int(nchunks), int(ws)) == (0, 8192, 1, ref.workspace_bytes)
+    assert out[1].split()[0] == "1"
+
+
 def _fake(addr=1 << 20):
     return addr  # an aligned, never dereferenced address
 
