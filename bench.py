@@ -227,7 +227,7 @@ def main():
     ap.add_argument("--chunk-rows", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline field (0 disables)")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--ref-rows", type=int, default=16,
                     help="rows per step of the reference (oracle) arm")
     ap.add_argument("--ce-bt", type=int, default=8192,

@@ -52,7 +52,9 @@ def test_flce_bf16_shapes(shape, red):
     compare(out, ref, "bf16", f"flce bf16 {shape} {red}")
 
 
-@pytest.mark.parametrize("chunk,acc", [(64, False), (128, False), (7, True), (1, True)])
+# 256-row chunks: grad_weight contractions 256 deep run as CTA pairs
+@pytest.mark.parametrize("chunk,acc", [(64, False), (128, False), (7, True), (1, True),
+                                       (256, False), (256, True)])
 def test_flce_chunking(chunk, acc):
     x, w, labels = jsd_inputs.make_ce_inputs(300, 64, 5000, "bf16", 103, ignore_frac=0.1)
     out, run = _gpu(x, w, labels, "bf16", chunk_rows=chunk, accum_fp32=acc)
