@@ -56,17 +56,21 @@ __device__ __forceinline__ MD md_combine(MD a, MD b) {
                    (b.m == -INFINITY ? 0.f : b.d * ex2(b.m - m))};
 }
 
-// Block-wide (m, d) and sum in a fixed order (deterministic): butterflies in
-// each warp, then one butterfly over the per-warp results in warp 0, whose
-// total every thread reads from the slot after theirs (shm, shs hold
-// kWarps + 1).
+// Block-wide (m, d) and sum in a fixed order (deterministic): inside each
+// warp, then over the per-warp results in warp 0, whose total every thread
+// reads from the slot after theirs (shm, shs hold kWarps + 1). In a warp: the
+// largest m in one instruction (exact, so order-free), every lane's d
+// rescaled to it, and d and s summed in a fixed butterfly order.
 __device__ __forceinline__ void warp_md_sum(MD& v, float& s) {
+  float m;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v.m));
+  float2 ds = make_float2(m == -INFINITY ? 0.f : v.d * ex2(v.m - m), s);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    MD u{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.d, o)};
-    v = md_combine(v, u);
-    s += __shfl_xor_sync(0xffffffffu, s, o);
-  }
+  for (int o = 16; o > 0; o >>= 1)
+    ds = __fadd2_rn(ds, make_float2(__shfl_xor_sync(0xffffffffu, ds.x, o),
+                                    __shfl_xor_sync(0xffffffffu, ds.y, o)));
+  v = MD{m, ds.x};
+  s = ds.y;
 }
 __device__ __forceinline__ void block_md2(MD& v, float& s, MD* shm, float* shs) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -159,7 +163,8 @@ __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
     const bool have_stats = (a.stats != nullptr) && !CAP;
     if (have_stats) {
       const float2* ps = a.stats + r * a.ntiles;
-      for (int64_t i = threadIdx.x; i < a.ntiles; i += blockDim.x)
+      if ((int64_t)threadIdx.x < a.ntiles) md = MD{ps[threadIdx.x].x, ps[threadIdx.x].y};
+      for (int64_t i = threadIdx.x + blockDim.x; i < a.ntiles; i += blockDim.x)
         md = md_combine(md, MD{ps[i].x, ps[i].y});
     } else {
       for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {

@@ -59,24 +59,39 @@ __device__ __forceinline__ void md_fold(MD& s, const float (&z)[N], float c) {
   s.d += acc;
 }
 
-// Block-wide reductions in a fixed order (deterministic): a butterfly inside
-// each warp, the per-warp results through shared memory, a butterfly over
-// them in warp 0, and the total broadcast from the slot after theirs.
-__device__ __forceinline__ MD warp_md(MD v) {
+// Block-wide reductions in a fixed order (deterministic): inside each warp,
+// then over the per-warp results in warp 0, the total broadcast from the slot
+// after theirs.
+__device__ __forceinline__ float2 warp_sum2(float2 v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    MD u{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.d, o)};
-    v = md_combine(v, u);
-  }
+  for (int o = 16; o > 0; o >>= 1)
+    v = __fadd2_rn(v, make_float2(__shfl_xor_sync(0xffffffffu, v.x, o),
+                                  __shfl_xor_sync(0xffffffffu, v.y, o)));
   return v;
+}
+// Largest value over the warp in one instruction (exact, so order-free).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+// The student's and the teacher's (m, d) over a warp: the warp's largest m,
+// every lane's d rescaled to it, and those summed in a fixed butterfly order
+// (one ex2 a lane instead of one per butterfly level).
+__device__ __forceinline__ void warp_md2(MD& a, MD& b) {
+  const float ma = warp_max(a.m), mb = warp_max(b.m);
+  float2 d = make_float2(ma == -CUDART_INF_F ? 0.f : a.d * ex2(a.m - ma),
+                         mb == -CUDART_INF_F ? 0.f : b.d * ex2(b.m - mb));
+  d = warp_sum2(d);
+  a = MD{ma, d.x};
+  b = MD{mb, d.y};
 }
 // The student's and the teacher's (m, d) together: one pair of barriers.
 // sh holds 2 * (NW + 1).
 template <int NW>
 __device__ __forceinline__ void block_md2(MD& va, MD& vb, MD* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  va = warp_md(va);
-  vb = warp_md(vb);
+  warp_md2(va, vb);
   if (lane == 0) {
     sh[2 * warp] = va;
     sh[2 * warp + 1] = vb;
@@ -85,8 +100,7 @@ __device__ __forceinline__ void block_md2(MD& va, MD& vb, MD* sh) {
   if (warp == 0) {
     MD ua = lane < NW ? sh[2 * lane] : MD{-CUDART_INF_F, 0.f};
     MD ub = lane < NW ? sh[2 * lane + 1] : MD{-CUDART_INF_F, 0.f};
-    ua = warp_md(ua);
-    ub = warp_md(ub);
+    warp_md2(ua, ub);
     if (lane == 0) {
       sh[2 * NW] = ua;
       sh[2 * NW + 1] = ub;
@@ -97,14 +111,6 @@ __device__ __forceinline__ void block_md2(MD& va, MD& vb, MD* sh) {
   vb = sh[2 * NW + 1];
 }
 
-__device__ __forceinline__ float2 warp_sum2(float2 v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-  }
-  return v;
-}
 template <int NW>
 __device__ __forceinline__ float2 block_sum2(float2 v, float2* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -244,7 +250,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_jsd_rows(JsdRowArgs a) {
       // the logits GEMM already folded each 128 columns of this row
       const float2* ps = a.stats_s + r * a.ntiles;
       const float2* pt = a.stats_t + r * a.ntiles;
-      for (int64_t i = threadIdx.x; i < a.ntiles; i += blockDim.x) {
+      if ((int64_t)threadIdx.x < a.ntiles) {  // a thread's first partial as it is
+        const float2 u = ps[threadIdx.x], w2 = pt[threadIdx.x];
+        ma = MD{u.x, u.y};
+        mb = MD{w2.x, w2.y};
+      }
+      for (int64_t i = threadIdx.x + blockDim.x; i < a.ntiles; i += blockDim.x) {
         const float2 u = ps[i], w2 = pt[i];
         ma = md_combine(ma, MD{u.x, u.y});
         mb = md_combine(mb, MD{w2.x, w2.y});
