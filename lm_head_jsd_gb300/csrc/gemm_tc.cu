@@ -223,6 +223,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
                    (g.d32 != nullptr && (g.accumulate || g.finalize));
   const char* penv = getenv("FLJSD_GEMM_PREFETCH");
   const bool pf_off = penv != nullptr && penv[0] == '0';
+  bool two_groups = false;  // a second epilogue group chosen with the slab ring
   if (rmw && p.k_splits == 1 && !pf_off) {
     const bool f32 = g.d32 != nullptr;
     const void* src = f32 ? (const void*)g.d32 : g.d;
@@ -247,6 +248,18 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
         if (p.num_k_blocks <= 4) {
           p.nst = pair ? 3 : 2;
           p.nslab = 8;
+        } else if (pair && !f32 && p.num_k_blocks <= 8) {
+          // K = 320..512 on CTA pairs, bf16 D: four stages and a ring of six
+          // slabs fit next to a second epilogue group (measured, grad_weight
+          // ms per headline step against 4 / 5 / one group: K = 384 9.08 vs
+          // 10.73, K = 512 7.58 vs 8.64; at K = 256, 640, 768 and 1024 the
+          // rules around this one stay faster). Six entries are enough for
+          // two groups here: a bf16 slab is 64 columns, two per group and
+          // tile, so a warp's next slab is at most three ring positions past
+          // the one it still holds back, and no wait can close a cycle.
+          p.nst = 4;
+          p.nslab = 6;
+          two_groups = true;
         } else if (p.num_k_blocks <= 16) {
           p.nst = pair ? 4 : 3;
           p.nslab = 5;
@@ -271,14 +284,16 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   // Two epilogue groups where the epilogue bounds the tile (a short
   // contraction per unit: measured ~0.4 us per 32-column chunk and warp, a
   // latency chain that one warp per scheduler cannot hide). A slab ring then
-  // needs 8 entries: with one release deferred per warp, two groups can hold
-  // back up to 5 entries of the fp32 ring (3 of the bf16 one). Measured on
+  // needs more than the entries that two groups can hold back with one
+  // release deferred per warp: 5 of the fp32 ring (8 entries), 3 of the bf16
+  // one (6 or 8 entries, the rules above). Measured on
   // 128256 x 4096 outputs (same box, against one group): read-modify-write
   // 431 -> 320 us at K = 128; write-only 233 -> 190 us at K = 128, even at
   // K = 192, but 244 -> 301 us at K = 256, where the fourth operand stage
   // that the second group's staging buffers displace matters more.
   p.epi_groups = 1;
-  if ((p.nslab == 8 && p.kb_per_split <= 4) || (p.nslab == 0 && p.kb_per_split <= 3)) {
+  if (two_groups || (p.nslab == 8 && p.kb_per_split <= 4) ||
+      (p.nslab == 0 && p.kb_per_split <= 3)) {
     p.epi_groups = 2;
     if (p.stage_out) p.nst = pair ? 5 : 3;  // room for 8 warps x 2 staging buffers
   }

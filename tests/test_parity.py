@@ -418,13 +418,16 @@ def test_fp32_grad_weight_accumulation(chunk, monkeypatch):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("chunk", [1024, 384, 320])
 @pytest.mark.parametrize("accum_fp32", [False, True], ids=["bf16_rmw", "fp32_acc"])
-def test_chunked_grad_weight_on_cta_pairs(accum_fp32, monkeypatch):
-    """Chunks of 1024 rows make grad_weight a K = 1024 contraction, deep
+def test_chunked_grad_weight_on_cta_pairs(accum_fp32, chunk, monkeypatch):
+    """Chunks of 1024, 384 or 320 rows make grad_weight a contraction deep
     enough for the CTA-pair schedule, so later chunks add into grad_weight (or
     the fp32 accumulator) through the pair kernel's read-modify-write epilogue
     (PR 1429 "Summary": first chunk overwrites, later chunks add and round
-    once). Against the oracle, and bitwise against one CTA per tile."""
+    once); at 384 and 320 rows the bf16 one runs two epilogue groups on a
+    six-slab ring, and the last chunk is shorter. Against the oracle, and
+    bitwise against one CTA per tile."""
     from lm_head_jsd_gb300 import FusedLinearJSD
 
     w = jsd_inputs.custom("pairchunks", 43, 3072, 64, 5000, "bf16", ignore_frac=0.1)
@@ -434,12 +437,12 @@ def test_chunked_grad_weight_on_cta_pairs(accum_fp32, monkeypatch):
     outs = []
     for pair in ("1", "0"):
         monkeypatch.setenv("FLJSD_GEMM_PAIR", pair)
-        run = FusedLinearJSD(3072, 64, 64, 5000, torch.bfloat16, chunk_rows=1024,
+        run = FusedLinearJSD(3072, 64, 64, 5000, torch.bfloat16, chunk_rows=chunk,
                              accum_fp32=accum_fp32)
-        assert run.plan.num_chunks == 3
+        assert run.plan.num_chunks == -(-3072 // chunk)
         outs.append([t.clone() for t in run.forward(x_s, w_s, x_t, w_t, labels)])
         torch.cuda.synchronize()
-    compare(outs[0], ref, "bf16", f"pair chunks accum_fp32={accum_fp32}",
+    compare(outs[0], ref, "bf16", f"pair chunks {chunk} accum_fp32={accum_fp32}",
             zeros=oracle_zeros(inputs, 0.5, 1.0))
     for a, b in zip(outs[0], outs[1]):
         assert torch.equal(a, b)
