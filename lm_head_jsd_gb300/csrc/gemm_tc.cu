@@ -143,7 +143,22 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   const bool pair_off = penv_pair != nullptr && penv_pair[0] == '0';
   const bool pair_any = penv_pair != nullptr && penv_pair[0] == '2';
   const bool deep = (g.k + BK - 1) / BK >= 4;
-  const bool pair = mblocks >= 2 && splits <= 1 && !g.single_cta && !pair_off && (deep || pair_any);
+  // Waves of tiles over the GPU: pairs run ceil(mblocks / 2) 256-row tiles per
+  // n-block on half as many clusters, so an odd m-block count leaves a pair
+  // half empty and a small tile count can need one wave more. Pairs are kept
+  // while their waves are at most 12% more than one CTA per tile needs (about
+  // what a pair's halved B copies save per tile). Measured, ms per headline
+  // step at 384 / 640 / 896 / 1152-row chunks, pairs vs one CTA: logits
+  // 15.0 / 12.1 / 12.0 / 10.8 vs 13.1 / 11.7 / 11.5 / 11.6 (waves 14 / 20 / 27
+  // / 33 vs 10 / 17 / 24 / 30); grad_input at 1152 rows 8.9 vs 5.4 (2 waves vs
+  // 1), at 640 and 896 rows 7.9 and 6.1 vs 8.6 and 6.6 (1 wave each).
+  const int64_t nblocks = (g.n + BN - 1) / BN;
+  const int64_t sms = num_sms();
+  const int64_t waves_one = (mblocks * nblocks + sms - 1) / sms;
+  const int64_t waves_pair = ((mblocks + 1) / 2 * nblocks + sms / 2 - 1) / (sms / 2);
+  const bool waves_ok = waves_pair * 100 <= waves_one * 112;
+  const bool pair = mblocks >= 2 && splits <= 1 && !g.single_cta && !pair_off &&
+                    ((deep && waves_ok) || pair_any);
   CUtensorMap ma, mb;
   bool ok;
   if (g.a_mn)  // A stored [k x m]
