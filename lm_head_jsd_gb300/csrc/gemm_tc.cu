@@ -154,8 +154,9 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t st) {
   // 1), at 640 and 896 rows 7.9 and 6.1 vs 8.6 and 6.6 (1 wave each).
   const int64_t nblocks = (g.n + BN - 1) / BN;
   const int64_t sms = num_sms();
+  const int64_t clusters = sms >= 2 ? sms / 2 : 1;
   const int64_t waves_one = (mblocks * nblocks + sms - 1) / sms;
-  const int64_t waves_pair = ((mblocks + 1) / 2 * nblocks + sms / 2 - 1) / (sms / 2);
+  const int64_t waves_pair = ((mblocks + 1) / 2 * nblocks + clusters - 1) / clusters;
   const bool waves_ok = waves_pair * 100 <= waves_one * 112;
   const bool pair = mblocks >= 2 && splits <= 1 && !g.single_cta && !pair_off &&
                     ((deep && waves_ok) || pair_any);
