@@ -229,7 +229,10 @@ fljsd_status fljsd_gemm_bf16(const void* a, int64_t lda, int32_t a_mn, const voi
 /* flags of fljsd_gemm_bf16: by default, for contractions at least 256 deep,
  * pairs of 128-row blocks of D run as CTA pairs (2-CTA clusters,
  * tcgen05.mma.cta_group::2) that compute a 256 x 256 tile together, each CTA
- * copying only its own rows of A and half of the B tile;
+ * copying only its own rows of A and half of the B tile, unless the pairs
+ * would need more than 12% more waves of tiles over the GPU than one CTA per
+ * tile (an odd block count leaves a pair half empty; few tiles can add a
+ * wave);
  * FLJSD_GEMM_SINGLE_CTA runs one CTA per 128 x 256 tile. The results are
  * identical. The environment variable FLJSD_GEMM_PAIR (read at each launch)
  * selects for every GEMM of the library: 0 one CTA per tile, 2 CTA pairs at
