@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
     float csum2 = 0.f;
     if constexpr (!CAP && sizeof(T) == 2) {
       // bf16 without a cap: kCeUnroll vectors per iteration with bulk L2
-      // prefetches two iterations ahead; the label's element is corrected once, by the
+      // prefetches three iterations ahead; the label's element is corrected once, by the
       // thread whose vector holds it; the sum of c only where label smoothing
       // needs it; packed fp32x2 arithmetic (each lane rounds as the scalar form)
       const int step = (int)blockDim.x, nv = (int)nvec, chunk = kCeUnroll * step;
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
       const float2 nld2 = make_float2(-ld2, -ld2), gsm2 = make_float2(gsm, gsm);
       const float2 neps2 = make_float2(-eps_v, -eps_v), w2 = make_float2(w, w);
       if (threadIdx.x == 0)
-        l2_prefetch_span(zr, (size_t)(nv < 2 * chunk ? nv : 2 * chunk) * N * sizeof(T));
+        l2_prefetch_span(zr, (size_t)(nv < 3 * chunk ? nv : 3 * chunk) * N * sizeof(T));
       auto vec = [&](float (&zs)[N]) {
 #pragma unroll
         for (int k = 0; k < N; k += 2) {
@@ -246,9 +246,9 @@ __global__ void __launch_bounds__(kThreads) k_ce_rows(CeRowArgs a) {
       };
       int i = (int)threadIdx.x;
       for (; i + (kCeUnroll - 1) * step < nv; i += kCeUnroll * step) {
-        if (threadIdx.x == 0 && i + 2 * chunk < nv)
-          l2_prefetch_span(zr + (int64_t)(i + 2 * chunk) * N,
-                           (size_t)(nv - (i + 2 * chunk) < chunk ? nv - (i + 2 * chunk) : chunk) *
+        if (threadIdx.x == 0 && i + 3 * chunk < nv)
+          l2_prefetch_span(zr + (int64_t)(i + 3 * chunk) * N,
+                           (size_t)(nv - (i + 3 * chunk) < chunk ? nv - (i + 3 * chunk) : chunk) *
                                N * sizeof(T));
         uint4 raw[kCeUnroll];  // packed bf16: 4 registers a vector in flight
 #pragma unroll
