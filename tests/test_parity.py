@@ -191,6 +191,9 @@ SMALL = [
     (1, 8, 1, "bf16"), (1, 8, 7, "bf16"), (3, 16, 33, "bf16"), (130, 24, 1000, "bf16"),
     (257, 72, 4099, "bf16"), (1, 5, 1, "fp32"), (2, 7, 13, "fp32"), (65, 17, 1001, "fp32"),
     (129, 64, 9000, "bf16"),
+    # H not a multiple of 8: the bf16 contractions run on the CUDA cores and
+    # the row kernel forms pass 1 itself (no GEMM-epilogue partials)
+    (33, 12, 1000, "bf16"), (70, 100, 2051, "bf16"),
 ]
 
 
