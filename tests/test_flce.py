@@ -104,6 +104,22 @@ def test_flce_label_positions(eps, lam):
     assert rel_fro(f64(gw), gw_ref) <= tol_grad
 
 
+@pytest.mark.parametrize("ignore_index", [5, 0])
+def test_flce_custom_ignore_index(ignore_index):
+    """A class id as ignore_index: rows with that label are skipped (loss 0,
+    gradient rows exactly 0) and the mean divides by the other rows."""
+    x, w, labels = jsd_inputs.make_ce_inputs(80, 64, 2500, "bf16", 108)
+    labels[::4] = ignore_index
+    for red in ("mean", "none"):
+        out, _ = _gpu(x, w, labels, "bf16", reduction=red, ignore_index=ignore_index,
+                      label_smoothing=0.1)
+        ref = oracle.flce_ref(f64(x), f64(w), labels.numpy(), reduction=red,
+                              ignore_index=ignore_index, label_smoothing=0.1)
+        compare(out, ref, "bf16", f"flce ignore_index={ignore_index} {red}")
+        ign = (labels == ignore_index).numpy()
+        assert np.all(f64(out[1])[ign] == 0.0)
+
+
 def test_flce_invalid_label_is_reported():
     from lm_head_jsd_gb300 import fljsd_workspace_status
 

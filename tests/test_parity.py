@@ -212,6 +212,34 @@ def test_small_shapes(shape, beta):
             assert e <= TOL[dt][1], (shape, red, k, e)
 
 
+@pytest.mark.parametrize("ignore_index", [7, 0])
+def test_custom_ignore_index(ignore_index):
+    """Rows whose label equals the given ignore_index (not -100) are skipped
+    (loss 0, gradient rows exactly 0, n counts the rest); -100 is then an
+    ordinary label whose rows count."""
+    from lm_head_jsd_gb300 import FusedLinearJSD
+
+    bt, h, v = 96, 64, 3000
+    w = jsd_inputs.custom("ignidx", 51, bt, h, v, "bf16")
+    x_s, w_s, x_t, w_t, _ = jsd_inputs.make_inputs(w, "cpu")
+    labels = torch.randint(0, v, (bt,), generator=torch.Generator().manual_seed(52))
+    labels[1::7] = -100
+    labels[::5] = ignore_index
+    for red in ("batchmean", "none"):
+        run = FusedLinearJSD(bt, h, h, v, torch.bfloat16, beta=0.5, temperature=1.0,
+                             reduction=red, ignore_index=ignore_index, device="cuda:0")
+        out = run.forward(*(t.cuda() for t in (x_s, w_s, x_t, w_t, labels)))
+        torch.cuda.synchronize()
+        ref = oracle.fljsd_ref(f64(x_s), f64(w_s), f64(x_t), f64(w_t), labels.numpy(),
+                               beta=0.5, temperature=1.0, reduction=red,
+                               ignore_index=ignore_index)
+        compare(out, ref, "bf16", f"ignore_index={ignore_index} {red}")
+        ign = (labels == ignore_index).numpy()
+        assert np.all(f64(out[1])[ign] == 0.0)
+        if red == "none":
+            assert np.all(f64(out[0])[ign] == 0.0) and np.all(f64(out[0])[~ign] != 0.0)
+
+
 @pytest.mark.parametrize("chunk", [1, 7, 64, 128, 300])
 def test_chunking_accumulates_grad_weight(chunk):
     w = jsd_inputs.custom("chunks", 21, 300, 64, 5000, "bf16", ignore_frac=0.1)
