@@ -120,6 +120,25 @@ def test_generalized_matches_entropy_form(beta):
         assert loss_rows[r] == pytest.approx(ref, rel=1e-10, abs=1e-14)
 
 
+@pytest.mark.parametrize("T", [1.0, 2.0])
+def test_beta_half_is_library_jensen_shannon(T):
+    """At beta = 0.5 the generalized branch is the symmetric Jensen-Shannon
+    divergence, whose square root scipy.spatial.distance.jensenshannon
+    computes (natural log) from the two softmax distributions."""
+    from scipy.spatial.distance import jensenshannon
+
+    x_s, w_s, x_t, w_t = _problem(8, bt=5, h=16, v=300)
+    loss_rows, _, _ = fljsd_ref(x_s, w_s, x_t, w_t, beta=0.5, temperature=T, reduction="none")
+    zs = (x_s @ w_s.T) / T
+    zt = (x_t @ w_t.T) / T
+    q = np.exp(zs - zs.max(axis=1, keepdims=True))
+    q /= q.sum(axis=1, keepdims=True)
+    p = np.exp(zt - zt.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    for r in range(5):
+        assert loss_rows[r] == pytest.approx(jensenshannon(p[r], q[r]) ** 2, rel=1e-9)
+
+
 # ---------------------------------------------------------------------------
 # invariants
 # ---------------------------------------------------------------------------
