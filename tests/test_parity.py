@@ -212,6 +212,27 @@ def test_small_shapes(shape, beta):
             assert e <= TOL[dt][1], (shape, red, k, e)
 
 
+@pytest.mark.parametrize("v", [122880, 131072])
+def test_rows_longer_than_the_shared_cache(v):
+    """bf16 rows of more than 114,688 columns: the row kernel's pass 3 takes
+    X - log M of the first 114,688 from its shared-memory cache and recomputes
+    the rest of the row from both logits. Every element against the oracle,
+    tile edges included, and with the teacher equal to the student every
+    gradient exactly 0."""
+    w = jsd_inputs.custom("tmemrows", 61, 48, 64, v, "bf16", ignore_frac=0.1)
+    inputs = jsd_inputs.make_inputs(w, "cpu")
+    for red in ("batchmean", "none"):
+        out = run_gpu(*inputs, beta=0.5, temperature=1.0, reduction=red)
+        ref = _oracle(inputs, beta=0.5, temperature=1.0, reduction=red)
+        compare(out, ref, "bf16", f"V={v} {red}", zeros=oracle_zeros(inputs, 0.5, 1.0))
+        for k, e in tile_errors(f64(out[2]), ref[2], v).items():
+            assert e <= TOL["bf16"][1], (v, red, k, e)
+    x_s, w_s, _, _, labels = inputs
+    loss, gi, gw = run_gpu(x_s, w_s, x_s, w_s, labels, beta=0.5, temperature=1.0)
+    assert loss.item() == 0.0
+    assert int(torch.count_nonzero(gi)) == 0 and int(torch.count_nonzero(gw)) == 0
+
+
 @pytest.mark.parametrize("ignore_index", [7, 0])
 def test_custom_ignore_index(ignore_index):
     """Rows whose label equals the given ignore_index (not -100) are skipped
